@@ -1,0 +1,162 @@
+/*
+ * mcs.h — C ABI of libmcs: the MC-Sparse hot path on one NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the method described in "MC-Sparse: Deconstructing and
+ * Closing the Dense-Sparse Attention Gap in Diffusion Transformers" (summary
+ * page of arXiv 2610.06801). Paragraphs are cited by subject:
+ *   [grouping]  index gathering and PDDP: queries are cut into groups of exactly
+ *               C (the tile width) by projecting onto the principal direction,
+ *               splitting at the median and repeating; keys and values are
+ *               gathered from per-group index lists, not repacked into blocks;
+ *   [selection] the anchor step's two-pass exact top-K: per group, the K keys
+ *               with the largest summed attention weight; pass 1 is the row
+ *               max / log-sum-exp, pass 2 recomputes the probabilities;
+ *   [residual]  the anchor stores dense output minus sparse output; reuse steps
+ *               add it to a fresh sparse attention of the current Q, K, V;
+ *   [dense]     every anchor still runs full dense attention.
+ *
+ * Conventions shared by every entry point
+ *   - Tensors q, k, v, o, residual are contiguous [B, H, N, d] with d fastest
+ *     (row-major, one row per token), element type given by mcs_desc.dtype.
+ *     N is the number of real tokens; N_pad = G*C with G = ceil(N/C) groups.
+ *   - perm is int32 [B, H, N_pad]: for each (b, h), token ids listed group by
+ *     group (group g occupies perm[g*C .. g*C+C-1]), ascending inside a group.
+ *     Entries >= N are pad slots (zero queries; their outputs are never written).
+ *   - group_of is int32 [B, H, N]: the group id of each real token.
+ *   - idx is int32 [B, H, G, K]: per group, K key ids in [0, N), ascending.
+ *   - lse is fp32 [B, H, N]: natural-log row log-sum-exp of the scaled logits.
+ *   - Every pointer is a DEVICE pointer unless stated otherwise, owned by the
+ *     caller, 16-byte aligned, and must stay valid until the stream reaches the
+ *     call. Inputs may not alias outputs.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream). Argument errors are returned before anything is launched.
+ *     A failed launch returns MCS_ERR_CUDA. Faults detected on the device (an
+ *     index out of range) do not stop the kernel: the offending row is skipped,
+ *     a sticky flag is raised, and mcs_check_status() reports it.
+ *   - The library allocates no device memory except one small static word of
+ *     device status flags; all scratch space is the caller's workspace.
+ *   - No C++ exception crosses this boundary.
+ */
+#ifndef MCS_H_
+#define MCS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *mcs_stream; /* same type as cudaStream_t */
+
+typedef enum {
+  MCS_OK = 0,
+  MCS_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad size, K out of [1, N] */
+  MCS_ERR_UNSUPPORTED = 2,    /* d, C or dtype outside the supported set */
+  MCS_ERR_WORKSPACE = 3,      /* workspace pointer null or smaller than mcs_workspace_size() */
+  MCS_ERR_CUDA = 4,           /* a CUDA runtime call or kernel launch failed */
+  MCS_ERR_DEVICE_BOUNDS = 5,  /* a kernel met an index outside [0, N) (reported by mcs_check_status) */
+  MCS_ERR_DEVICE_TIMEOUT = 6  /* a kernel's bounded wait ran out and it stopped early */
+} mcs_status;
+
+typedef enum { MCS_F32 = 0, MCS_BF16 = 1 } mcs_dtype;
+
+/* Problem description. Supported: d in {64, 128}; C in {64, 128}; dtype F32 or
+ * BF16 (BF16 runs on the tcgen05 tensor cores with fp32 accumulation, F32 runs
+ * in fp32 SIMT arithmetic); B*H*N_pad < 2^31. scale <= 0 selects 1/sqrt(d).
+ * pddp_iters <= 0 selects 20 power iterations. */
+typedef struct {
+  int B, H, N, d, C;
+  int dtype;       /* mcs_dtype */
+  float scale;
+  int pddp_iters;
+} mcs_desc;
+
+/* Bytes of device workspace that mcs_group_pddp and mcs_anchor_select need for
+ * this problem and this K (the larger of the two). Returns 0 for an invalid
+ * description. Host-only; launches nothing. */
+size_t mcs_workspace_size(const mcs_desc *desc, int K);
+
+/* [grouping] PDDP grouping of each head's queries into G groups of exactly C.
+ * Per (b, h) and per tree node of n >= 2 groups: mean of the node's real
+ * queries, principal direction of the centred node by exactly pddp_iters power
+ * iterations from 1/sqrt(d)*ones, projection of each member, and a rank split
+ * sending the floor(n/2)*C members with the lowest (projection, token id) left.
+ * Pads (ids >= N) sort last. Group ids are the depth-first leaf order.
+ * q: [B,H,N,d]. Writes perm [B,H,N_pad] and group_of [B,H,N].
+ * ws/ws_bytes: caller-owned device scratch, at least mcs_workspace_size(desc, 1)
+ * bytes; its contents on entry are ignored. */
+mcs_status mcs_group_pddp(const mcs_desc *desc, const void *q, int32_t *perm, int32_t *group_of,
+                          void *ws, size_t ws_bytes, mcs_stream stream);
+
+/* [dense] + [selection] pass 1: full softmax attention of every query over every
+ * key, o_i = sum_j softmax_j(scale q_i.k_j) v_j, and the row log-sum-exp.
+ * q, k, v: [B,H,N,d] inputs; o: [B,H,N,d] output (may be NULL to compute only
+ * lse); lse: fp32 [B,H,N] output (may be NULL). At least one must be non-NULL. */
+mcs_status mcs_dense_attn(const mcs_desc *desc, const void *q, const void *k, const void *v,
+                          void *o, float *lse, mcs_stream stream);
+
+/* [selection] pass 2 + exact top-K. For every group g: S_g[j] = sum over the
+ * group's real queries i of exp(scale q_i.k_j - lse_i); idx[g] = the K keys with
+ * the largest S_g (ties to the lower key id), written ascending.
+ * perm: [B,H,N_pad] from mcs_group_pddp. lse: fp32 [B,H,N] from
+ * mcs_dense_attn, or NULL to have pass 1 computed here (into the workspace).
+ * idx: int32 [B,H,G,K] output. mass: fp32 [B,H,G] output or NULL; mass[g] =
+ * sum_{j in idx[g]} S_g[j] / (real queries in g). ws: at least
+ * mcs_workspace_size(desc, K) bytes. */
+mcs_status mcs_anchor_select(const mcs_desc *desc, const void *q, const void *k, const int32_t *perm,
+                             const float *lse, int K, int32_t *idx, float *mass,
+                             void *ws, size_t ws_bytes, mcs_stream stream);
+
+/* [grouping] + [residual] token-gather sparse attention. For every group g and
+ * real member i: o_i = sum_{j in idx[g]} softmax_{idx[g]}(scale q_i.k_j) v_j
+ * (renormalised over the kept keys), plus residual_i when residual != NULL.
+ * Rows are read through perm and written back to their token positions; pad
+ * slots are skipped. q, k, v: current-step [B,H,N,d]; idx: [B,H,G,K];
+ * residual: [B,H,N,d] or NULL; o: [B,H,N,d] output. */
+mcs_status mcs_sparse_attn_gather(const mcs_desc *desc, const void *q, const void *k, const void *v,
+                                  const int32_t *perm, const int32_t *idx, int K,
+                                  const void *residual, void *o, mcs_stream stream);
+
+/* [residual] anchor residual in one pass: the sparse attention of
+ * mcs_sparse_attn_gather (without residual) is computed and r_i = o_dense_i -
+ * o_sparse_i is written, in fp32 and rounded once to dtype. o_dense: [B,H,N,d]
+ * from mcs_dense_attn; r: [B,H,N,d] output. */
+mcs_status mcs_anchor_residual(const mcs_desc *desc, const void *q, const void *k, const void *v,
+                               const int32_t *perm, const int32_t *idx, int K,
+                               const void *o_dense, void *r, mcs_stream stream);
+
+/* [residual] r = o_dense - o_sparse, element-wise over [B,H,N,d]. */
+mcs_status mcs_residual_store(const mcs_desc *desc, const void *o_dense, const void *o_sparse, void *r,
+                              mcs_stream stream);
+
+/* [residual] o = o_sparse + r, element-wise over [B,H,N,d]. o may equal o_sparse. */
+mcs_status mcs_residual_apply(const mcs_desc *desc, const void *o_sparse, const void *r, void *o,
+                              mcs_stream stream);
+
+/* Synchronises `stream`, then reports (and clears) the device-side flags raised
+ * since the last call: MCS_ERR_DEVICE_BOUNDS, MCS_ERR_DEVICE_TIMEOUT, or a
+ * sticky CUDA error as MCS_ERR_CUDA. MCS_OK if none. */
+mcs_status mcs_check_status(mcs_stream stream);
+
+/* Static, NUL-terminated description of a status code. Never NULL. */
+const char *mcs_status_string(mcs_status status);
+
+/* Number of kernels this process has launched through the library so far
+ * (host-side counter, for launch accounting). */
+uint64_t mcs_launch_count(void);
+
+/* Diagnostic (no counterpart in the method): one tcgen05 MMA chain
+ * D[128 x 128] = A[128 x 64] * B on the tensor cores, to check the shared-memory
+ * descriptor encodings the attention kernels rely on. a: bf16 [128 x 64]
+ * row-major; mode 0: b is bf16 [128 x 64] row-major (K-major operand,
+ * D = A B^T); mode 1: b is bf16 [64 x 128] row-major (MN-major operand, D = A B)
+ * with the descriptor's leading/stride byte offsets mn_lbo / mn_sbo. d: fp32
+ * [128 x 128] output. All device pointers. */
+mcs_status mcs_selftest_tc_mma(const void *a, const void *b, float *d, int mode, uint32_t mn_lbo, uint32_t mn_sbo,
+                               mcs_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MCS_H_ */

@@ -1,0 +1,393 @@
+// C ABI of libmcs (declared in include/mcs.h): argument validation, workspace
+// layout, dispatch to the bf16 tcgen05 kernels or the fp32 SIMT kernels, and
+// the device status word. Nothing here allocates device memory.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "mcs.h"
+#include "attn_tc.h"
+#include "common.cuh"
+#include "kernels.h"
+#include "status.cuh"
+
+namespace {
+
+__device__ uint32_t g_status_word;  // OR of mcs::kStatus* bits raised by kernels
+std::atomic<uint64_t> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+uint32_t* g_status_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+// Rows of pass-2 scores kept in the workspace at once (each row is N fp32).
+constexpr long long kSelectRows = 4096;
+
+struct Dims {
+  int B, H, N, d, C, G, N_pad, BH;
+  bool bf16;
+  float scale;
+  int iters;
+};
+
+mcs_status check_desc(const mcs_desc* desc, Dims* o) {
+  if (desc == nullptr) return MCS_ERR_INVALID_ARG;
+  if (desc->B < 1 || desc->H < 1 || desc->N < 1) return MCS_ERR_INVALID_ARG;
+  if (desc->d != 64 && desc->d != 128) return MCS_ERR_UNSUPPORTED;
+  if (desc->C != 64 && desc->C != 128) return MCS_ERR_UNSUPPORTED;
+  if (desc->dtype != MCS_F32 && desc->dtype != MCS_BF16) return MCS_ERR_UNSUPPORTED;
+  if (!std::isfinite(desc->scale)) return MCS_ERR_INVALID_ARG;
+  const long long G = (static_cast<long long>(desc->N) + desc->C - 1) / desc->C;
+  const long long BH = static_cast<long long>(desc->B) * desc->H;
+  if (BH > 65535 || BH * G * desc->C >= (1ll << 31)) return MCS_ERR_UNSUPPORTED;
+  o->B = desc->B;
+  o->H = desc->H;
+  o->N = desc->N;
+  o->d = desc->d;
+  o->C = desc->C;
+  o->G = static_cast<int>(G);
+  o->N_pad = static_cast<int>(G * desc->C);
+  o->BH = static_cast<int>(BH);
+  o->bf16 = desc->dtype == MCS_BF16;
+  o->scale = desc->scale > 0.f ? desc->scale : 1.0f / std::sqrt(static_cast<float>(desc->d));
+  o->iters = desc->pddp_iters > 0 ? desc->pddp_iters : 20;
+  return MCS_OK;
+}
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned16_or_null(const void* p) { return p == nullptr || aligned16(p); }
+
+mcs_status device_state(uint32_t** status, int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MCS_ERR_CUDA;
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return MCS_ERR_CUDA;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MCS_ERR_CUDA;
+    g_num_sms[dev] = n;
+    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  *status = g_status_ptr[dev];
+  if (sms) *sms = g_num_sms[dev];
+  return MCS_OK;
+}
+
+mcs_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MCS_OK : MCS_ERR_CUDA; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Anchor-select workspace: [lse fp32 BH*N] [score rows: min(BH*G, kSelectRows) * N fp32]
+size_t select_ws_bytes(const Dims& d) {
+  const long long rows = std::min<long long>(static_cast<long long>(d.BH) * d.G, kSelectRows);
+  return align256(size_t(d.BH) * d.N * 4) + align256(size_t(rows) * d.N * 4);
+}
+
+mcs_status dense_impl(const Dims& dm, const void* q, const void* k, const void* v, void* o, float* lse,
+                      uint32_t* status, cudaStream_t s) {
+  if (dm.bf16) {
+    mcs::TcAttnParams p{};
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k = static_cast<const __nv_bfloat16*>(k);
+    p.v = static_cast<const __nv_bfloat16*>(v);
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.lse = lse;
+    p.N = dm.N;
+    p.N_pad = dm.N_pad;
+    p.C = dm.C;
+    p.G = dm.G;
+    p.K = dm.N;
+    p.tiles_per_head = (dm.N + 127) / 128;
+    p.scale_log2 = dm.scale * mcs::kLog2e;
+    p.status = status;
+    return from_cuda(mcs::tc_dense_attn(dm.d, p, dm.BH, o != nullptr, s));
+  }
+  mcs::SimtAttnParams p{};
+  p.q = static_cast<const float*>(q);
+  p.k = static_cast<const float*>(k);
+  p.v = static_cast<const float*>(v);
+  p.o = static_cast<float*>(o);
+  p.lse = lse;
+  p.N = dm.N;
+  p.N_pad = dm.N_pad;
+  p.C = dm.C;
+  p.G = dm.G;
+  p.K = dm.N;
+  p.d = dm.d;
+  p.scale = dm.scale;
+  p.status = status;
+  return from_cuda(mcs::simt_dense_attn(p, dm.BH, s));
+}
+
+mcs_status sparse_impl(const Dims& dm, int epi, const void* q, const void* k, const void* v, const int32_t* perm,
+                       const int32_t* idx, int K, const void* res_in, void* o, void* res_out, uint32_t* status,
+                       cudaStream_t s) {
+  if (dm.bf16) {
+    mcs::TcAttnParams p{};
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k = static_cast<const __nv_bfloat16*>(k);
+    p.v = static_cast<const __nv_bfloat16*>(v);
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.perm = perm;
+    p.idx = idx;
+    p.res_in = static_cast<const __nv_bfloat16*>(res_in);
+    p.res_out = static_cast<__nv_bfloat16*>(res_out);
+    p.N = dm.N;
+    p.N_pad = dm.N_pad;
+    p.C = dm.C;
+    p.G = dm.G;
+    p.K = K;
+    p.tiles_per_head = dm.G;
+    p.scale_log2 = dm.scale * mcs::kLog2e;
+    p.status = status;
+    return from_cuda(mcs::tc_sparse_attn(dm.d, epi, p, dm.BH, s));
+  }
+  mcs::SimtAttnParams p{};
+  p.q = static_cast<const float*>(q);
+  p.k = static_cast<const float*>(k);
+  p.v = static_cast<const float*>(v);
+  p.o = static_cast<float*>(o);
+  p.perm = perm;
+  p.idx = idx;
+  p.res_in = static_cast<const float*>(res_in);
+  p.res_out = static_cast<float*>(res_out);
+  p.N = dm.N;
+  p.N_pad = dm.N_pad;
+  p.C = dm.C;
+  p.G = dm.G;
+  p.K = K;
+  p.d = dm.d;
+  p.scale = dm.scale;
+  p.status = status;
+  return from_cuda(mcs::simt_sparse_attn(epi, p, dm.BH, s));
+}
+
+}  // namespace
+
+namespace mcs {
+void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
+}  // namespace mcs
+
+extern "C" {
+
+size_t mcs_workspace_size(const mcs_desc* desc, int K) {
+  Dims dm;
+  if (check_desc(desc, &dm) != MCS_OK) return 0;
+  (void)K;
+  const size_t a = mcs::pddp_workspace_bytes(dm.BH, dm.N_pad, dm.C, dm.G, dm.d, dm.bf16);
+  const size_t b = select_ws_bytes(dm);
+  return a > b ? a : b;
+}
+
+mcs_status mcs_group_pddp(const mcs_desc* desc, const void* q, int32_t* perm, int32_t* group_of, void* ws,
+                          size_t ws_bytes, mcs_stream stream) {
+  Dims dm;
+  mcs_status st = check_desc(desc, &dm);
+  if (st != MCS_OK) return st;
+  if (!aligned16(q) || !aligned16(perm) || !aligned16(group_of)) return MCS_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned16(ws) || ws_bytes < mcs_workspace_size(desc, 1)) return MCS_ERR_WORKSPACE;
+  uint32_t* status = nullptr;
+  if ((st = device_state(&status, nullptr)) != MCS_OK) return st;
+  mcs::PddpProblem p{};
+  p.q = q;
+  p.perm = perm;
+  p.group_of = group_of;
+  p.BH = dm.BH;
+  p.N = dm.N;
+  p.N_pad = dm.N_pad;
+  p.C = dm.C;
+  p.G = dm.G;
+  p.d = dm.d;
+  p.iters = dm.iters;
+  p.bf16 = dm.bf16;
+  p.status = status;
+  return from_cuda(mcs::pddp_run(p, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mcs_status mcs_dense_attn(const mcs_desc* desc, const void* q, const void* k, const void* v, void* o, float* lse,
+                          mcs_stream stream) {
+  Dims dm;
+  mcs_status st = check_desc(desc, &dm);
+  if (st != MCS_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return MCS_ERR_INVALID_ARG;
+  if (o == nullptr && lse == nullptr) return MCS_ERR_INVALID_ARG;
+  if (!aligned16_or_null(o) || !aligned16_or_null(lse)) return MCS_ERR_INVALID_ARG;
+  uint32_t* status = nullptr;
+  if ((st = device_state(&status, nullptr)) != MCS_OK) return st;
+  return dense_impl(dm, q, k, v, o, lse, status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+mcs_status mcs_anchor_select(const mcs_desc* desc, const void* q, const void* k, const int32_t* perm, const float* lse,
+                             int K, int32_t* idx, float* mass, void* ws, size_t ws_bytes, mcs_stream stream) {
+  Dims dm;
+  mcs_status st = check_desc(desc, &dm);
+  if (st != MCS_OK) return st;
+  if (K < 1 || K > dm.N) return MCS_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(perm) || !aligned16(idx)) return MCS_ERR_INVALID_ARG;
+  if (!aligned16_or_null(lse) || !aligned16_or_null(mass)) return MCS_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned16(ws) || ws_bytes < mcs_workspace_size(desc, K)) return MCS_ERR_WORKSPACE;
+  uint32_t* status = nullptr;
+  if ((st = device_state(&status, nullptr)) != MCS_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  float* ws_lse = reinterpret_cast<float*>(w);
+  float* scores = reinterpret_cast<float*>(w + align256(size_t(dm.BH) * dm.N * 4));
+  if (lse == nullptr) {
+    // pass 1 computed here: row max / log-sum-exp only (no P V product)
+    st = dense_impl(dm, q, k, k, nullptr, ws_lse, status, s);
+    if (st != MCS_OK) return st;
+    lse = ws_lse;
+  }
+  const long long total = static_cast<long long>(dm.BH) * dm.G;
+  for (long long r0 = 0; r0 < total; r0 += kSelectRows) {
+    const int nrows = static_cast<int>(std::min<long long>(kSelectRows, total - r0));
+    cudaError_t e;
+    if (dm.bf16) {
+      mcs::TcColsumParams p{};
+      p.q = static_cast<const __nv_bfloat16*>(q);
+      p.k = static_cast<const __nv_bfloat16*>(k);
+      p.perm = perm;
+      p.lse = lse;
+      p.scores = scores;
+      p.N = dm.N;
+      p.N_pad = dm.N_pad;
+      p.C = dm.C;
+      p.G = dm.G;
+      p.row0 = static_cast<int>(r0);
+      p.scale_log2 = dm.scale * mcs::kLog2e;
+      p.status = status;
+      e = mcs::tc_colsum(dm.d, dm.C, p, nrows, s);
+    } else {
+      mcs::SimtColsumParams p{};
+      p.q = static_cast<const float*>(q);
+      p.k = static_cast<const float*>(k);
+      p.perm = perm;
+      p.lse = lse;
+      p.scores = scores;
+      p.N = dm.N;
+      p.N_pad = dm.N_pad;
+      p.C = dm.C;
+      p.G = dm.G;
+      p.d = dm.d;
+      p.row0 = static_cast<int>(r0);
+      p.scale = dm.scale;
+      p.status = status;
+      e = mcs::simt_colsum(p, nrows, s);
+    }
+    if (e != cudaSuccess) return MCS_ERR_CUDA;
+    mcs::TopkParams t{};
+    t.scores = scores;
+    t.perm = perm;
+    t.idx = idx;
+    t.mass = mass;
+    t.N = dm.N;
+    t.N_pad = dm.N_pad;
+    t.C = dm.C;
+    t.G = dm.G;
+    t.K = K;
+    t.row0 = static_cast<int>(r0);
+    t.status = status;
+    if ((e = mcs::topk_rows(t, nrows, s)) != cudaSuccess) return MCS_ERR_CUDA;
+  }
+  return MCS_OK;
+}
+
+mcs_status mcs_sparse_attn_gather(const mcs_desc* desc, const void* q, const void* k, const void* v,
+                                  const int32_t* perm, const int32_t* idx, int K, const void* residual, void* o,
+                                  mcs_stream stream) {
+  Dims dm;
+  mcs_status st = check_desc(desc, &dm);
+  if (st != MCS_OK) return st;
+  if (K < 1 || K > dm.N) return MCS_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(perm) || !aligned16(idx) || !aligned16(o))
+    return MCS_ERR_INVALID_ARG;
+  if (!aligned16_or_null(residual)) return MCS_ERR_INVALID_ARG;
+  uint32_t* status = nullptr;
+  if ((st = device_state(&status, nullptr)) != MCS_OK) return st;
+  return sparse_impl(dm, residual ? mcs::kEpiAddResidual : mcs::kEpiPlain, q, k, v, perm, idx, K, residual, o,
+                     nullptr, status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+mcs_status mcs_anchor_residual(const mcs_desc* desc, const void* q, const void* k, const void* v, const int32_t* perm,
+                               const int32_t* idx, int K, const void* o_dense, void* r, mcs_stream stream) {
+  Dims dm;
+  mcs_status st = check_desc(desc, &dm);
+  if (st != MCS_OK) return st;
+  if (K < 1 || K > dm.N) return MCS_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(perm) || !aligned16(idx) ||
+      !aligned16(o_dense) || !aligned16(r))
+    return MCS_ERR_INVALID_ARG;
+  uint32_t* status = nullptr;
+  if ((st = device_state(&status, nullptr)) != MCS_OK) return st;
+  return sparse_impl(dm, mcs::kEpiStoreResidual, q, k, v, perm, idx, K, o_dense, nullptr, r, status,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+mcs_status mcs_residual_store(const mcs_desc* desc, const void* o_dense, const void* o_sparse, void* r,
+                              mcs_stream stream) {
+  Dims dm;
+  mcs_status st = check_desc(desc, &dm);
+  if (st != MCS_OK) return st;
+  if (!aligned16(o_dense) || !aligned16(o_sparse) || !aligned16(r)) return MCS_ERR_INVALID_ARG;
+  uint32_t* status = nullptr;
+  int sms = 0;
+  if ((st = device_state(&status, &sms)) != MCS_OK) return st;
+  const size_t n = size_t(dm.BH) * dm.N * dm.d;
+  return from_cuda(mcs::residual_op(true, dm.bf16, o_dense, o_sparse, r, n, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mcs_status mcs_residual_apply(const mcs_desc* desc, const void* o_sparse, const void* r, void* o, mcs_stream stream) {
+  Dims dm;
+  mcs_status st = check_desc(desc, &dm);
+  if (st != MCS_OK) return st;
+  if (!aligned16(o_sparse) || !aligned16(r) || !aligned16(o)) return MCS_ERR_INVALID_ARG;
+  uint32_t* status = nullptr;
+  int sms = 0;
+  if ((st = device_state(&status, &sms)) != MCS_OK) return st;
+  const size_t n = size_t(dm.BH) * dm.N * dm.d;
+  return from_cuda(mcs::residual_op(false, dm.bf16, o_sparse, r, o, n, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mcs_status mcs_check_status(mcs_stream stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MCS_ERR_CUDA;
+  uint32_t* status = nullptr;
+  mcs_status st = device_state(&status, nullptr);
+  if (st != MCS_OK) return st;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MCS_ERR_CUDA;
+  if (v != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return MCS_ERR_CUDA;
+  }
+  if (v & mcs::kStatusTimeout) return MCS_ERR_DEVICE_TIMEOUT;
+  if (v & mcs::kStatusBounds) return MCS_ERR_DEVICE_BOUNDS;
+  return MCS_OK;
+}
+
+const char* mcs_status_string(mcs_status status) {
+  switch (status) {
+    case MCS_OK: return "ok";
+    case MCS_ERR_INVALID_ARG: return "invalid argument";
+    case MCS_ERR_UNSUPPORTED: return "unsupported problem size or dtype";
+    case MCS_ERR_WORKSPACE: return "workspace missing or too small";
+    case MCS_ERR_CUDA: return "CUDA runtime error";
+    case MCS_ERR_DEVICE_BOUNDS: return "device kernel met an out-of-range index";
+    case MCS_ERR_DEVICE_TIMEOUT: return "device kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+uint64_t mcs_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+mcs_status mcs_selftest_tc_mma(const void* a, const void* b, float* d, int mode, uint32_t mn_lbo, uint32_t mn_sbo,
+                               mcs_stream stream) {
+  if (!aligned16(a) || !aligned16(b) || !aligned16(d) || (mode != 0 && mode != 1)) return MCS_ERR_INVALID_ARG;
+  uint32_t* status = nullptr;
+  mcs_status st = device_state(&status, nullptr);
+  if (st != MCS_OK) return st;
+  return from_cuda(mcs::tc_probe(a, b, d, mode, mn_lbo, mn_sbo, status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

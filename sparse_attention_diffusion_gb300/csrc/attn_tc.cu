@@ -1,0 +1,729 @@
+// tcgen05 (5th-generation tensor core) attention kernels for bf16 inputs on sm_103a.
+//
+//  * attn_tc_kernel: one CTA computes softmax attention for one tile of 128
+//    query rows. Dense mode walks every key of the head in tiles of 128;
+//    sparse mode gathers the group's queries through perm and walks the group's
+//    K selected keys, fetched row by row from the index list (keys are gathered,
+//    not repacked into blocks) [MC-Sparse summary: index-gather / PDDP paragraph].
+//    S = Q K^T and O += P V run on the tensor core with fp32 accumulators in
+//    tensor memory; the softmax (online, base-2, lazily rescaled) runs on the
+//    CUDA cores, one thread per query row.
+//  * colsum_tc_kernel: pass 2 of the anchor selection. For one query group it
+//    forms the transposed logits S^T = K_tile Q_g^T (the key on the TMEM lane),
+//    so each thread owns one key and sums exp(s - lse) over the group's queries
+//    without cross-thread reduction [MC-Sparse summary: anchor two-pass paragraph].
+//
+// Warp roles (288 threads): warps 0-3 softmax / column sums (thread = TMEM lane),
+// warp 4 tensor-memory allocation and the single MMA-issuing thread, warps 5-8
+// producers (cp.async row gathers into 128-byte-swizzled shared memory).
+// Every wait is bounded; on a timeout the CTA raises a status flag, drains its
+// in-flight copies and MMAs, frees tensor memory and returns.
+#include <cstdio>
+
+#include "attn_tc.h"
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace mcs {
+namespace {
+
+constexpr int kThreads = 288;
+constexpr int kRegion = 128 * 128;  // one 128-byte-swizzled region: 128 rows x 128 B
+
+// Byte offset of the 16-byte chunk `ch` (8 bf16 along the contiguous dim) of row
+// `row` inside a [rows x 64*nregions] tile stored as 128B-swizzled regions.
+__device__ __forceinline__ uint32_t sw128_off(int row, int ch) {
+  return uint32_t((ch >> 3) * kRegion + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
+}
+
+// K-major operand (rows = M or N, contiguous dim = K): k-step s covers K elements
+// [16s, 16s+16): region s/4, +32 B per step inside the 128-byte swizzle atom.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int s) {
+  return smem_desc_sw128(base + uint32_t((s >> 2) * kRegion + (s & 3) * 32), 16, 1024);
+}
+// MN-major operand (contiguous dim = N, rows = K): k-step s covers rows [16s, 16s+16).
+// Leading byte offset = stride between 64-element N chunks (one region),
+// stride byte offset = stride between groups of 8 rows.
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int s) {
+  return smem_desc_sw128(base + uint32_t(s * 16 * 128), kRegion, 1024);
+}
+
+__device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
+
+template <int D>
+struct AttnSmem {
+  static constexpr int kTile = (D / 64) * kRegion;   // [128 x D] bf16
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kTile;              // 2 stages
+  static constexpr int kV = kK + 2 * kTile;          // 2 stages
+  static constexpr int kP = kV + 2 * kTile;          // [128 x 128] bf16
+  static constexpr int kBar = kP + 2 * kRegion;
+  static constexpr int kNumBars = 18;
+  static constexpr int kMisc = kBar + kNumBars * 8;  // tmem slot, abort flag
+  static constexpr int kTok = kMisc + 16;            // q tokens [128], k tokens [2][128], v tokens [2][128]
+  static constexpr int kBytes = kTok + 5 * 128 * 4;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+template <int D, bool kSparse, int kEpi, bool kPV>
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcAttnParams p) {
+  using L = AttnSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;   // [2]
+  uint64_t* k_empty = bars + 3;  // [2]
+  uint64_t* v_full = bars + 5;   // [2]
+  uint64_t* v_empty = bars + 7;  // [2]
+  uint64_t* s_full = bars + 9;   // [2]
+  uint64_t* s_free = bars + 11;  // [2]
+  uint64_t* p_full = bars + 13;
+  uint64_t* p_empty = bars + 14;
+  uint64_t* o_done = bars + 15;
+  uint64_t* drain = bars + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  int32_t* q_tok = reinterpret_cast<int32_t*>(smem + L::kTok);
+  int32_t* k_tok = q_tok + 128;
+  int32_t* v_tok = q_tok + 384;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.y, tile = blockIdx.x;
+  const int nkv = kSparse ? p.K : p.N;
+  const int T = (nkv + 127) / 128;
+  uint32_t* st = p.status;
+
+  if (tid == 0) {
+    mbar_init(q_full, 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(k_full + s, 64);
+      mbar_init(k_empty + s, 1);
+      mbar_init(v_full + s, 64);
+      mbar_init(v_empty + s, 1);
+      mbar_init(s_full + s, 1);
+      mbar_init(s_free + s, 128);
+    }
+    mbar_init(p_full, 128);
+    mbar_init(p_empty, 1);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem;          // two S buffers: columns [0,128) and [128,256)
+  const uint32_t tO = tmem + 256;    // O accumulator: columns [256, 256+D)
+
+  if (warp >= 5) {
+    // ------------------------------------------------------------ producers
+    const int pt = tid - 160;  // 0..127
+    // Q tile: row r holds token q_tok[r] (or zeros).
+    {
+      int tok = -1;
+      if constexpr (kSparse) {
+        if (pt < p.C) {
+          const int t = p.perm[size_t(bh) * p.N_pad + size_t(tile) * p.C + pt];
+          if (t < 0 || t >= p.N_pad) raise_status(st, kStatusBounds);
+          else if (t < p.N) tok = t;
+        }
+      } else {
+        const int t = tile * 128 + pt;
+        if (t < p.N) tok = t;
+      }
+      q_tok[pt] = tok;
+      named_bar_sync(1, 128);
+      const __nv_bfloat16* qb = p.q + size_t(bh) * p.N * D;
+#pragma unroll 4
+      for (int it = 0; it < D / 8; ++it) {
+        const int id = it * 128 + pt, row = id / (D / 8), ch = id % (D / 8);
+        const int t = q_tok[row];
+        cp_async16(sbase + L::kQ + sw128_off(row, ch), qb + size_t(t < 0 ? 0 : t) * D + ch * 8, t >= 0);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      mbar_arrive(q_full);
+    }
+    // K (threads 0-63) and V (threads 64-127) pipelines.
+    const bool isK = pt < 64;
+    const int gt = pt & 63;
+    if (isK || kPV) {
+      uint64_t* full = isK ? k_full : v_full;
+      uint64_t* empty = isK ? k_empty : v_empty;
+      int32_t* toks = isK ? k_tok : v_tok;
+      const __nv_bfloat16* src = (isK ? p.k : p.v) + size_t(bh) * p.N * D;
+      const uint32_t sm = sbase + (isK ? L::kK : L::kV);
+      const uint32_t bar_id = isK ? 2 : 3;
+      const int32_t* idxg = kSparse ? p.idx + (size_t(bh) * p.G + tile) * size_t(p.K) : nullptr;
+      volatile int* grp_stop = abort_flag + (isK ? 1 : 2);  // written by the group leader only
+      int j = 0;
+      for (; j < T; ++j) {
+        const int s = j & 1;
+        const uint32_t u = uint32_t(j) >> 1;
+        if (gt == 0) {
+          int stop = *abort_flag;
+          if (!stop && !mbar_wait(empty + s, (u & 1) ^ 1, st)) {
+            raise_status(st, kStatusTimeout);
+            *abort_flag = 1;
+            stop = 1;
+          }
+          *grp_stop = stop;
+        }
+        named_bar_sync(bar_id, 64);
+        if (*grp_stop) break;
+        for (int r = gt; r < 128; r += 64) {
+          const int slot = j * 128 + r;
+          int tok = -1;
+          if (slot < nkv) {
+            const int t = kSparse ? idxg[slot] : slot;
+            if (t < 0 || t >= p.N) raise_status(st, kStatusBounds);
+            else tok = t;
+          }
+          toks[s * 128 + r] = tok;
+        }
+        named_bar_sync(bar_id, 64);
+#pragma unroll 4
+        for (int it = 0; it < 2 * D / 8; ++it) {
+          const int id = it * 64 + gt, row = id / (D / 8), ch = id % (D / 8);
+          const int t = toks[s * 128 + row];
+          cp_async16(sm + s * L::kTile + sw128_off(row, ch), src + size_t(t < 0 ? 0 : t) * D + ch * 8, t >= 0);
+        }
+        cp_async_commit();
+        if (j >= 1) {
+          cp_async_wait<1>();
+          fence_proxy_async_smem();
+          mbar_arrive(full + ((j - 1) & 1));
+        }
+      }
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      if (j == T && T > 0) mbar_arrive(full + ((T - 1) & 1));
+    }
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
+      bool ok = mbar_wait(q_full, 0, st);
+      bool issued = false;
+      auto issue_pv = [&](int i) -> bool {
+        const int s = i & 1;
+        const uint32_t u = uint32_t(i) >> 1;
+        if (!mbar_wait(v_full + s, u & 1, st)) return false;
+        if (!mbar_wait(p_full, uint32_t(i) & 1, st)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          tc_mma_ss(tO, desc_kmajor(sbase + L::kP, ks), desc_mnmajor(sbase + L::kV + s * L::kTile, ks), kIdescPV,
+                    (i > 0 || ks > 0) ? 1u : 0u);
+        tc_commit(p_empty);
+        tc_commit(v_empty + s);
+        return true;
+      };
+      for (int j = 0; ok && j < T; ++j) {
+        const int s = j & 1;
+        const uint32_t u = uint32_t(j) >> 1;
+        ok = mbar_wait(k_full + s, u & 1, st) && mbar_wait(s_free + s, (u & 1) ^ 1, st);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          tc_mma_ss(tS + s * 128, desc_kmajor(sbase + L::kQ, ks), desc_kmajor(sbase + L::kK + s * L::kTile, ks),
+                    kIdescQK, ks > 0 ? 1u : 0u);
+        tc_commit(s_full + s);
+        tc_commit(k_empty + s);
+        issued = true;
+        if (kPV && j >= 1) ok = issue_pv(j - 1);
+      }
+      if (ok && kPV && T > 0) ok = issue_pv(T - 1);
+      if (ok) tc_commit(o_done);
+      if (!ok) {
+        raise_status(st, kStatusTimeout);
+        *abort_flag = 1;
+        if (issued) {
+          tc_commit(drain);
+          mbar_wait(drain, 0, st);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax (thread = query row)
+    const int row = tid;
+    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    uint8_t* sP = smem + L::kP;
+    for (int j = 0; j < T; ++j) {
+      const int b = j & 1;
+      const uint32_t u = uint32_t(j) >> 1;
+      ok = warp_all(mbar_wait(s_full + b, u & 1, st));
+      if (!ok) break;
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tS + lane_off + b * 128 + c * 32, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+      }
+      tc_fence_before();
+      mbar_arrive(s_free + b);
+      const int nvalid = min(128, nkv - j * 128);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) mx = fmaxf(mx, c < nvalid ? s[c] : -INFINITY);
+      const float m_new = fmaxf(m, mx * p.scale_log2);
+      const bool need = m_new > m + 8.f;  // lazy rescale: keep a stale max unless it grew by > 2^8
+      if constexpr (kPV) {
+        ok = warp_all(mbar_wait(p_empty, (uint32_t(j) & 1) ^ 1, st));  // PV of tile j-1 done
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, need && j > 0)) {
+          const float alpha = (need && j > 0) ? ex2_approx(m - m_new) : 1.f;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tO + lane_off + c * 32, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(tO + lane_off + c * 32, r);
+          }
+        }
+      }
+      if (need) {
+        l *= ex2_approx(m - m_new);
+        m = m_new;
+      }
+      const float neg_m = -m;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        s[c] = c < nvalid ? ex2_approx(fmaf(s[c], p.scale_log2, neg_m)) : 0.f;
+        l += s[c];
+      }
+      if constexpr (kPV) {
+#pragma unroll
+        for (int c8 = 0; c8 < 16; ++c8) {
+          uint4 v;
+          v.x = pack_bf16x2(s[c8 * 8 + 0], s[c8 * 8 + 1]);
+          v.y = pack_bf16x2(s[c8 * 8 + 2], s[c8 * 8 + 3]);
+          v.z = pack_bf16x2(s[c8 * 8 + 4], s[c8 * 8 + 5]);
+          v.w = pack_bf16x2(s[c8 * 8 + 6], s[c8 * 8 + 7]);
+          *reinterpret_cast<uint4*>(sP + sw128_off(row, c8)) = v;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(p_full);
+      }
+    }
+    // ------------------------------------------------------------ epilogue
+    int tok = -1;
+    if constexpr (kSparse) {
+      if (row < p.C) {
+        const int t = p.perm[size_t(bh) * p.N_pad + size_t(tile) * p.C + row];
+        if (t >= 0 && t < p.N) tok = t;
+      }
+    } else {
+      const int t = tile * 128 + row;
+      if (t < p.N) tok = t;
+    }
+    if (ok && !kSparse && p.lse != nullptr && tok >= 0)
+      p.lse[size_t(bh) * p.N + tok] = (m + __log2f(l)) * kLn2;
+    if constexpr (kPV) {
+      if (ok) ok = warp_all(mbar_wait(o_done, 0, st));
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = 1.f / l;
+        const size_t rowoff = (size_t(bh) * p.N + size_t(tok < 0 ? 0 : tok)) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tO + lane_off + c * 32, r);
+          if (tok >= 0 && (kEpi == kEpiStoreResidual || p.o != nullptr)) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              float o8[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) o8[i] = __uint_as_float(r[q4 * 8 + i]) * inv_l;
+              const size_t off = rowoff + c * 32 + q4 * 8;
+              if constexpr (kEpi != kEpiPlain) {
+                const uint4 rv = *reinterpret_cast<const uint4*>(p.res_in + off);
+                const __nv_bfloat16* rb = reinterpret_cast<const __nv_bfloat16*>(&rv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  o8[i] = (kEpi == kEpiAddResidual) ? o8[i] + __bfloat162float(rb[i]) : __bfloat162float(rb[i]) - o8[i];
+              }
+              uint4 w;
+              w.x = pack_bf16x2(o8[0], o8[1]);
+              w.y = pack_bf16x2(o8[2], o8[3]);
+              w.z = pack_bf16x2(o8[4], o8[5]);
+              w.w = pack_bf16x2(o8[6], o8[7]);
+              __nv_bfloat16* dst = (kEpi == kEpiStoreResidual) ? p.res_out : p.o;
+              *reinterpret_cast<uint4*>(dst + off) = w;
+            }
+          }
+        }
+      }
+    }
+    if (!ok) {
+      raise_status(st, kStatusTimeout);
+      *abort_flag = 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- select pass 2
+template <int D, int CQ>
+struct ColsumSmem {
+  static constexpr int kTile = (D / 64) * kRegion;
+  static constexpr int kQ = 0;                 // [CQ x D] (stored with 128-row regions)
+  static constexpr int kK = kQ + kTile;        // 2 stages of [128 x D]
+  static constexpr int kBar = kK + 2 * kTile;
+  static constexpr int kNumBars = 10;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kLse = kMisc + 16;      // [CQ] fp32, log2 units
+  static constexpr int kTok = kLse + 128 * 4;  // q tokens [128], k tokens [2][128]
+  static constexpr int kBytes = kTok + 3 * 128 * 4;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+template <int D, int CQ>
+__global__ void __launch_bounds__(kThreads, 1) colsum_tc_kernel(const TcColsumParams p) {
+  using L = ColsumSmem<D, CQ>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;   // [2]
+  uint64_t* k_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;   // [2]
+  uint64_t* s_free = bars + 7;   // [2]
+  uint64_t* drain = bars + 9;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  float* lse2 = reinterpret_cast<float*>(smem + L::kLse);
+  int32_t* q_tok = reinterpret_cast<int32_t*>(smem + L::kTok);
+  int32_t* k_tok = q_tok + 128;
+
+  constexpr uint32_t kCols = CQ <= 64 ? 128 : 256;  // two S^T buffers of CQ columns
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int grow = p.row0 + blockIdx.x;  // global group row = bh * G + g
+  const int bh = grow / p.G, g = grow % p.G;
+  const int T = (p.N + 127) / 128;
+  uint32_t* st = p.status;
+
+  if (tid == 0) {
+    mbar_init(q_full, 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(k_full + s, 128);
+      mbar_init(k_empty + s, 1);
+      mbar_init(s_full + s, 1);
+      mbar_init(s_free + s, 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(tmem_slot, kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp >= 5) {
+    const int pt = tid - 160;
+    {
+      int tok = -1;
+      if (pt < p.C && pt < CQ) {
+        const int t = p.perm[size_t(bh) * p.N_pad + size_t(g) * p.C + pt];
+        if (t < 0 || t >= p.N_pad) raise_status(st, kStatusBounds);
+        else if (t < p.N) tok = t;
+      }
+      q_tok[pt] = tok;
+      named_bar_sync(1, 128);
+      const __nv_bfloat16* qb = p.q + size_t(bh) * p.N * D;
+      for (int it = 0; it < D / 8; ++it) {
+        const int id = it * 128 + pt, row = id / (D / 8), ch = id % (D / 8);
+        if (row < CQ) {
+          const int t = q_tok[row];
+          cp_async16(sbase + L::kQ + sw128_off(row, ch), qb + size_t(t < 0 ? 0 : t) * D + ch * 8, t >= 0);
+        }
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      mbar_arrive(q_full);
+    }
+    const __nv_bfloat16* kb = p.k + size_t(bh) * p.N * D;
+    volatile int* grp_stop = abort_flag + 1;  // written by the producer leader only
+    int j = 0;
+    for (; j < T; ++j) {
+      const int s = j & 1;
+      const uint32_t u = uint32_t(j) >> 1;
+      if (pt == 0) {
+        int stop = *abort_flag;
+        if (!stop && !mbar_wait(k_empty + s, (u & 1) ^ 1, st)) {
+          raise_status(st, kStatusTimeout);
+          *abort_flag = 1;
+          stop = 1;
+        }
+        *grp_stop = stop;
+      }
+      named_bar_sync(1, 128);
+      if (*grp_stop) break;
+#pragma unroll 4
+      for (int it = 0; it < D / 8; ++it) {
+        const int id = it * 128 + pt, row = id / (D / 8), ch = id % (D / 8);
+        const int t = j * 128 + row;
+        cp_async16(sbase + L::kK + s * L::kTile + sw128_off(row, ch), kb + size_t(t < p.N ? t : 0) * D + ch * 8,
+                   t < p.N);
+      }
+      cp_async_commit();
+      if (j >= 1) {
+        cp_async_wait<1>();
+        fence_proxy_async_smem();
+        mbar_arrive(k_full + ((j - 1) & 1));
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    if (j == T && T > 0) mbar_arrive(k_full + ((T - 1) & 1));
+  } else if (warp == 4) {
+    if (lane == 0) {
+      constexpr uint32_t kIdesc = idesc_bf16_f32(128, CQ, 0, 0);
+      bool ok = mbar_wait(q_full, 0, st);
+      bool issued = false;
+      for (int j = 0; ok && j < T; ++j) {
+        const int s = j & 1;
+        const uint32_t u = uint32_t(j) >> 1;
+        ok = mbar_wait(k_full + s, u & 1, st) && mbar_wait(s_free + s, (u & 1) ^ 1, st);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          tc_mma_ss(tmem + s * CQ, desc_kmajor(sbase + L::kK + s * L::kTile, ks), desc_kmajor(sbase + L::kQ, ks),
+                    kIdesc, ks > 0 ? 1u : 0u);
+        tc_commit(s_full + s);
+        tc_commit(k_empty + s);
+        issued = true;
+      }
+      if (!ok) {
+        raise_status(st, kStatusTimeout);
+        *abort_flag = 1;
+        if (issued) {
+          tc_commit(drain);
+          mbar_wait(drain, 0, st);
+        }
+      }
+    }
+  } else {
+    // thread = key lane of the current 128-key tile
+    if (tid < CQ) {
+      int t = -1;
+      if (tid < p.C) {
+        const int v = p.perm[size_t(bh) * p.N_pad + size_t(g) * p.C + tid];
+        if (v >= 0 && v < p.N) t = v;
+      }
+      lse2[tid] = t >= 0 ? p.lse[size_t(bh) * p.N + t] * kLog2e : INFINITY;
+    }
+    named_bar_sync(4, 128);
+    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    float* out = p.scores + size_t(blockIdx.x) * p.N;
+    for (int j = 0; j < T; ++j) {
+      const int b = j & 1;
+      const uint32_t u = uint32_t(j) >> 1;
+      if (!warp_all(mbar_wait(s_full + b, u & 1, st))) {
+        raise_status(st, kStatusTimeout);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      float acc = 0.f;
+#pragma unroll
+      for (int c = 0; c < CQ / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + b * CQ + c * 32, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          acc += ex2_approx(fmaf(__uint_as_float(r[i]), p.scale_log2, -lse2[c * 32 + i]));
+      }
+      tc_fence_before();
+      mbar_arrive(s_free + b);
+      const int key = j * 128 + tid;
+      if (key < p.N) out[key] = acc;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kCols);
+  }
+}
+
+// ---------------------------------------------------------------- probe GEMM (self-test)
+// D[128 x N] = A[128 x 64] * B, one MMA chain of 4 k-steps, for checking the
+// descriptor encodings: mode 0: B given as [N x 64] K-major; mode 1: B given as
+// [64 x N] MN-major (N contiguous). lbo/sbo of the MN-major descriptor are inputs.
+__global__ void __launch_bounds__(128, 1) tc_probe_kernel(const __nv_bfloat16* a, const __nv_bfloat16* b, float* d,
+                                                          int mode, uint32_t mn_lbo, uint32_t mn_sbo,
+                                                          uint32_t* status) {
+  __shared__ __align__(1024) uint8_t sA[kRegion];
+  __shared__ __align__(1024) uint8_t sB[2 * kRegion];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t slot;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  constexpr int N = 128;
+  // A: 128 rows x 64 (K) -> one region
+  for (int id = tid; id < 128 * 8; id += 128) {
+    const int row = id >> 3, ch = id & 7;
+    *reinterpret_cast<uint4*>(sA + sw128_off(row, ch)) = *reinterpret_cast<const uint4*>(a + row * 64 + ch * 8);
+  }
+  if (mode == 0) {  // B: N rows x 64 (K) -> one region
+    for (int id = tid; id < N * 8; id += 128) {
+      const int row = id >> 3, ch = id & 7;
+      *reinterpret_cast<uint4*>(sB + sw128_off(row, ch)) = *reinterpret_cast<const uint4*>(b + row * 64 + ch * 8);
+    }
+  } else {  // B: 64 rows (K) x N (contiguous) -> N/64 regions, rows of 128 B
+    for (int id = tid; id < 64 * (N / 8); id += 128) {
+      const int row = id / (N / 8), ch = id % (N / 8);
+      *reinterpret_cast<uint4*>(sB + sw128_off(row, ch)) = *reinterpret_cast<const uint4*>(b + row * N + ch * 8);
+    }
+  }
+  fence_proxy_async_smem();
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&slot, 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = slot;
+  if (tid == 0) {
+    const uint32_t sa = smem_u32(sA), sb = smem_u32(sB);
+    for (int ks = 0; ks < 4; ++ks) {
+      const uint64_t da = desc_kmajor(sa, ks);
+      uint64_t db;
+      uint32_t idesc;
+      if (mode == 0) {
+        db = desc_kmajor(sb, ks);
+        idesc = idesc_bf16_f32(128, N, 0, 0);
+      } else {
+        db = smem_desc_sw128(sb + ks * 16 * 128, mn_lbo, mn_sbo);
+        idesc = idesc_bf16_f32(128, N, 0, 1);
+      }
+      tc_mma_ss(tmem, da, db, idesc, ks > 0 ? 1u : 0u);
+    }
+    tc_commit(&bar);
+  }
+  const bool ok = mbar_wait(&bar, 0, status);
+  if (!ok && tid == 0) raise_status(status, kStatusTimeout);
+  __syncwarp();
+  if (__all_sync(0xffffffffu, ok)) {
+    tc_fence_after();
+    for (int c = 0; c < N / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + c * 32, r);
+      for (int i = 0; i < 32; ++i) d[tid * N + c * 32 + i] = __uint_as_float(r[i]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, int bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- host launchers
+template <int D, bool kSparse, int kEpi, bool kPV>
+static cudaError_t launch_attn(const TcAttnParams& p, int BH, cudaStream_t stream) {
+  using L = AttnSmem<D>;
+  auto kern = attn_tc_kernel<D, kSparse, kEpi, kPV>;
+  cudaError_t e = set_smem(kern, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.tiles_per_head, BH);
+  kern<<<grid, kThreads, L::kAlloc, stream>>>(p);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t tc_dense_attn(int D, const TcAttnParams& p, int BH, bool with_pv, cudaStream_t stream) {
+  if (D == 128) return with_pv ? launch_attn<128, false, kEpiPlain, true>(p, BH, stream)
+                               : launch_attn<128, false, kEpiPlain, false>(p, BH, stream);
+  if (D == 64) return with_pv ? launch_attn<64, false, kEpiPlain, true>(p, BH, stream)
+                              : launch_attn<64, false, kEpiPlain, false>(p, BH, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t tc_sparse_attn(int D, int epi, const TcAttnParams& p, int BH, cudaStream_t stream) {
+#define MCS_SPARSE_CASE(DD, EE) \
+  if (D == DD && epi == EE) return launch_attn<DD, true, EE, true>(p, BH, stream);
+  MCS_SPARSE_CASE(128, kEpiPlain)
+  MCS_SPARSE_CASE(128, kEpiAddResidual)
+  MCS_SPARSE_CASE(128, kEpiStoreResidual)
+  MCS_SPARSE_CASE(64, kEpiPlain)
+  MCS_SPARSE_CASE(64, kEpiAddResidual)
+  MCS_SPARSE_CASE(64, kEpiStoreResidual)
+#undef MCS_SPARSE_CASE
+  return cudaErrorInvalidValue;
+}
+
+template <int D, int CQ>
+static cudaError_t launch_colsum(const TcColsumParams& p, int nrows, cudaStream_t stream) {
+  using L = ColsumSmem<D, CQ>;
+  auto kern = colsum_tc_kernel<D, CQ>;
+  cudaError_t e = set_smem(kern, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  kern<<<nrows, kThreads, L::kAlloc, stream>>>(p);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t tc_colsum(int D, int C, const TcColsumParams& p, int nrows, cudaStream_t stream) {
+  if (D == 128 && C == 128) return launch_colsum<128, 128>(p, nrows, stream);
+  if (D == 128 && C == 64) return launch_colsum<128, 64>(p, nrows, stream);
+  if (D == 64 && C == 128) return launch_colsum<64, 128>(p, nrows, stream);
+  if (D == 64 && C == 64) return launch_colsum<64, 64>(p, nrows, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t tc_probe(const void* a, const void* b, float* d, int mode, uint32_t lbo, uint32_t sbo, uint32_t* status,
+                     cudaStream_t stream) {
+  tc_probe_kernel<<<1, 128, 0, stream>>>(static_cast<const __nv_bfloat16*>(a), static_cast<const __nv_bfloat16*>(b),
+                                         d, mode, lbo, sbo, status);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace mcs

@@ -1,0 +1,69 @@
+// Host-side interface of the non-tensor-core kernels: residual, top-K, PDDP and
+// the fp32 SIMT attention path.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mcs {
+
+// ---------------------------------------------------------------- residual
+cudaError_t residual_op(bool store, bool bf16, const void* a, const void* b, void* out, size_t nelem, int num_sms,
+                        cudaStream_t s);
+
+// ---------------------------------------------------------------- top-K
+struct TopkParams {
+  const float* scores;   // [nrows, N] score rows of this launch
+  const int32_t* perm;   // [BH, N_pad] (for the real-query count of the mass)
+  int32_t* idx;          // [BH*G, K]
+  float* mass;           // [BH*G] or null
+  int N, N_pad, C, G, K;
+  int row0;              // first global group row of this launch
+  uint32_t* status;
+};
+cudaError_t topk_rows(const TopkParams& p, int nrows, cudaStream_t stream);
+
+// ---------------------------------------------------------------- PDDP
+struct PddpProblem {
+  const void* q;         // [BH, N, d] (fp32 or bf16)
+  int32_t* perm;         // [BH, N_pad] output
+  int32_t* group_of;     // [BH, N] output
+  int BH, N, N_pad, C, G, d, iters;
+  bool bf16;
+  uint32_t* status;
+};
+// Workspace bytes for pddp_run (0 if unsupported).
+size_t pddp_workspace_bytes(int BH, int N_pad, int C, int G, int d, bool bf16);
+cudaError_t pddp_run(const PddpProblem& p, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+// ---------------------------------------------------------------- fp32 SIMT attention
+struct SimtAttnParams {
+  const float* q;
+  const float* k;
+  const float* v;
+  float* o;               // may be null (lse only, dense)
+  float* lse;             // dense: [BH, N]; may be null
+  const int32_t* perm;    // sparse
+  const int32_t* idx;     // sparse
+  const float* res_in;    // add-residual: R; store-residual: o_dense
+  float* res_out;         // store-residual: R
+  int N, N_pad, C, G, K, d;
+  float scale;
+  uint32_t* status;
+};
+cudaError_t simt_dense_attn(const SimtAttnParams& p, int BH, cudaStream_t stream);
+cudaError_t simt_sparse_attn(int epi, const SimtAttnParams& p, int BH, cudaStream_t stream);
+
+struct SimtColsumParams {
+  const float* q;
+  const float* k;
+  const int32_t* perm;
+  const float* lse;
+  float* scores;          // [nrows, N]
+  int N, N_pad, C, G, d, row0;
+  float scale;
+  uint32_t* status;
+};
+cudaError_t simt_colsum(const SimtColsumParams& p, int nrows, cudaStream_t stream);
+
+}  // namespace mcs

@@ -1,0 +1,511 @@
+// PDDP query grouping on the GPU [MC-Sparse summary: PDDP paragraph: project the
+// queries onto their principal direction, split at the median, repeat, giving
+// groups of exactly C].
+//
+// Every head is processed at once, one tree level per round of launches. The
+// tree shape depends only on G: a node of n groups splits into floor(n/2) and
+// n - floor(n/2) groups, so node k of level l is found by walking the bits of
+// k from the root. The current ordering `perm` keeps every node's members in a
+// contiguous, ascending run; a level
+//   1. sums the members of each chunk (<= 8 groups of one node) -> node mean,
+//   2. accumulates each chunk's centred covariance (d x d) -> node covariance,
+//   3. runs exactly `iters` power iterations w = Cov v, v = w/|w| from 1/sqrt(d),
+//   4. projects every member on v and turns the projection into an
+//      order-preserving integer key (pads get the largest key),
+//   5. radix-selects the rank floor(n/2)*C key of each node and stably
+//      partitions the run: smaller keys (ties: earlier, i.e. lower token id) left.
+// All reductions run in a fixed order, so a run is deterministic. fp32 inputs
+// accumulate in fp64 end to end; bf16 inputs accumulate in fp32.
+#include <cmath>
+#include <vector>
+
+#include "block_scan.cuh"
+#include "common.cuh"
+#include "kernels.h"
+#include "status.cuh"
+
+namespace mcs {
+namespace {
+
+constexpr int kChunkGroups = 8;  // groups per covariance chunk
+
+__host__ __device__ inline bool pddp_node(int G, int level, int k, int* start, int* n) {
+  int s = 0, m = G;
+  for (int b = level - 1; b >= 0; --b) {
+    if (m < 2) return false;
+    const int nl = m / 2;
+    if ((k >> b) & 1) {
+      s += nl;
+      m -= nl;
+    } else {
+      m = nl;
+    }
+  }
+  *start = s;
+  *n = m;
+  return true;
+}
+
+int num_levels(int G) {
+  int L = 0;
+  while ((1 << L) < G) ++L;
+  return L;
+}
+
+int host_level_chunks(int G, int level) {
+  int total = 0;
+  for (int k = 0; k < (1 << level); ++k) {
+    int s, n;
+    if (pddp_node(G, level, k, &s, &n) && n >= 2) total += (n + kChunkGroups - 1) / kChunkGroups;
+  }
+  return total;
+}
+
+struct Tables {
+  int* node_start;   // [L][G]
+  int* node_n;       // [L][G]: groups in the node, 0 when absent or a leaf
+  int* node_chunk0;  // [L][G]
+  int* node_nchunks; // [L][G]
+  int* chunk_node;   // [L][G]
+  int* chunk_g0;     // [L][G]
+  int* chunk_ng;     // [L][G]
+};
+
+__global__ void __launch_bounds__(1024) tables_kernel(Tables t, int G) {
+  __shared__ int warp_tot[32];
+  __shared__ int s_base;
+  const int level = blockIdx.x;
+  const int nodes = 1 << level;
+  if (threadIdx.x == 0) s_base = 0;
+  __syncthreads();
+  for (int k0 = 0; k0 < nodes; k0 += 1024) {
+    const int k = k0 + threadIdx.x;
+    int s = 0, n = 0;
+    const bool exists = k < nodes && pddp_node(G, level, k, &s, &n);
+    const bool active = exists && n >= 2;
+    const int nch = active ? (n + kChunkGroups - 1) / kChunkGroups : 0;
+    // exclusive prefix of nch over the block (nch <= G fits easily)
+    int pre = 0, tot = 0;
+    {
+      // scan of small integers via per-bit predicate counts would be wasteful; use warp scan + block sum
+      const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+      int incl = nch;
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      if (lane == 31) warp_tot[warp] = incl;
+      __syncthreads();
+      int wpre = 0;
+      for (int w = 0; w < 32; ++w) {
+        wpre += (w < warp) ? warp_tot[w] : 0;
+        tot += warp_tot[w];
+      }
+      pre = wpre + incl - nch;
+      __syncthreads();
+    }
+    const int c0 = s_base + pre;
+    if (k < nodes) {
+      const size_t o = size_t(level) * G + k;
+      t.node_start[o] = s;
+      t.node_n[o] = active ? n : 0;
+      t.node_chunk0[o] = c0;
+      t.node_nchunks[o] = nch;
+      for (int c = 0; c < nch; ++c) {
+        const size_t co = size_t(level) * G + c0 + c;
+        t.chunk_node[co] = k;
+        t.chunk_g0[co] = s + c * kChunkGroups;
+        t.chunk_ng[co] = min(kChunkGroups, n - c * kChunkGroups);
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) s_base += tot;
+    __syncthreads();
+  }
+}
+
+__global__ void init_perm_kernel(int32_t* perm, int N_pad, size_t total) {
+  for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < total; i += size_t(gridDim.x) * blockDim.x)
+    perm[i] = int32_t(i % N_pad);
+}
+
+__global__ void finalize_kernel(const int32_t* perm, int32_t* group_of, int N, int N_pad, int C, size_t total,
+                                uint32_t* status) {
+  for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < total; i += size_t(gridDim.x) * blockDim.x) {
+    const size_t bh = i / N_pad;
+    const int pos = int(i % N_pad);
+    const int t = perm[i];
+    if (t < 0 || t >= N_pad) {
+      raise_status(status, kStatusBounds);
+      continue;
+    }
+    if (t < N) group_of[bh * N + t] = pos / C;
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ float ld_f(const T* p) {
+  return to_f32(*p);
+}
+
+// 1. per-chunk sums of real members
+template <typename T, typename A, int D>
+__global__ void __launch_bounds__(256) sum_kernel(const T* __restrict__ x, const int32_t* __restrict__ perm, Tables t,
+                                                  int level, int N, int N_pad, int C, int G, A* psum, int* pcnt,
+                                                  int max_chunks) {
+  constexpr int kLanes = 256 / D;
+  __shared__ A part[256];
+  __shared__ int cnt_part[kLanes];
+  const int c = blockIdx.x, bh = blockIdx.y;
+  const size_t to = size_t(level) * G + c;
+  const int g0 = t.chunk_g0[to], ng = t.chunk_ng[to];
+  const int dim = threadIdx.x % D, rl = threadIdx.x / D;
+  const int32_t* pr = perm + size_t(bh) * N_pad + size_t(g0) * C;
+  const T* xb = x + size_t(bh) * N * D;
+  A acc = 0;
+  int cnt = 0;
+  for (int r = rl; r < ng * C; r += kLanes) {
+    const int tok = pr[r];
+    if (tok < N) {
+      acc += A(to_f32(xb[size_t(tok) * D + dim]));
+      ++cnt;
+    }
+  }
+  part[threadIdx.x] = acc;
+  if (dim == 0) cnt_part[rl] = cnt;
+  __syncthreads();
+  if (threadIdx.x < D) {
+    A s = 0;
+    for (int l = 0; l < kLanes; ++l) s += part[l * D + threadIdx.x];
+    psum[(size_t(bh) * max_chunks + c) * D + threadIdx.x] = s;
+  }
+  if (threadIdx.x == 0) {
+    int s = 0;
+    for (int l = 0; l < kLanes; ++l) s += cnt_part[l];
+    pcnt[size_t(bh) * max_chunks + c] = s;
+  }
+}
+
+// 2. node mean, start vector
+template <typename A, int D>
+__global__ void mean_kernel(Tables t, int level, int G, const A* psum, const int* pcnt, A* node_mu, A* node_v,
+                            int max_chunks) {
+  const int k = blockIdx.x, bh = blockIdx.y;
+  const size_t to = size_t(level) * G + k;
+  if (t.node_n[to] < 2) return;
+  const int c0 = t.node_chunk0[to], nc = t.node_nchunks[to];
+  A s = 0;
+  int cnt = 0;
+  for (int c = 0; c < nc; ++c) {
+    s += psum[(size_t(bh) * max_chunks + c0 + c) * D + threadIdx.x];
+    cnt += pcnt[size_t(bh) * max_chunks + c0 + c];
+  }
+  node_mu[(size_t(bh) * G + k) * D + threadIdx.x] = cnt > 0 ? s / A(cnt) : A(0);
+  node_v[(size_t(bh) * G + k) * D + threadIdx.x] = A(1) / sqrt(A(D));
+}
+
+// 3a. per-chunk centred covariance; thread (bi, bj) owns a TB x TB block.
+template <typename T, typename A, int D>
+__global__ void __launch_bounds__(256) cov_kernel(const T* __restrict__ x, const int32_t* __restrict__ perm, Tables t,
+                                                  int level, int N, int N_pad, int C, int G, const A* node_mu,
+                                                  A* pcov, int max_chunks) {
+  constexpr int TB = D / 16;
+  constexpr int RB = 32;
+  __shared__ A mu[D];
+  __shared__ A xs[RB][D];
+  const int c = blockIdx.x, bh = blockIdx.y;
+  const size_t to = size_t(level) * G + c;
+  const int node = t.chunk_node[to], g0 = t.chunk_g0[to], ng = t.chunk_ng[to];
+  if (threadIdx.x < D) mu[threadIdx.x] = node_mu[(size_t(bh) * G + node) * D + threadIdx.x];
+  const int bi = threadIdx.x / 16, bj = threadIdx.x % 16;
+  A acc[TB][TB];
+#pragma unroll
+  for (int i = 0; i < TB; ++i)
+#pragma unroll
+    for (int j = 0; j < TB; ++j) acc[i][j] = 0;
+  const int32_t* pr = perm + size_t(bh) * N_pad + size_t(g0) * C;
+  const T* xb = x + size_t(bh) * N * D;
+  const int rows = ng * C;
+  __syncthreads();
+  for (int r0 = 0; r0 < rows; r0 += RB) {
+    for (int e = threadIdx.x; e < RB * D; e += 256) {
+      const int rr = e / D, dd = e % D;
+      const int r = r0 + rr;
+      A val = 0;
+      if (r < rows) {
+        const int tok = pr[r];
+        if (tok < N) val = A(to_f32(xb[size_t(tok) * D + dd])) - mu[dd];
+      }
+      xs[rr][dd] = val;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int rr = 0; rr < RB; ++rr) {
+      A a[TB], b[TB];
+#pragma unroll
+      for (int i = 0; i < TB; ++i) {
+        a[i] = xs[rr][bi * TB + i];
+        b[i] = xs[rr][bj * TB + i];
+      }
+#pragma unroll
+      for (int i = 0; i < TB; ++i)
+#pragma unroll
+        for (int j = 0; j < TB; ++j) acc[i][j] += a[i] * b[j];
+    }
+    __syncthreads();
+  }
+  A* out = pcov + (size_t(bh) * max_chunks + c) * D * D;
+#pragma unroll
+  for (int i = 0; i < TB; ++i)
+#pragma unroll
+    for (int j = 0; j < TB; ++j) out[(bi * TB + i) * D + bj * TB + j] = acc[i][j];
+}
+
+// 3b. node covariance (fixed-order sum of its chunks) and the power iterations.
+template <typename A, int D>
+__global__ void __launch_bounds__(256) power_kernel(Tables t, int level, int G, const A* pcov, A* node_v, int iters,
+                                                    int max_chunks) {
+  extern __shared__ uint8_t dyn[];
+  A* cov = reinterpret_cast<A*>(dyn);  // [D][D]
+  A* v = cov + D * D;                  // [D]
+  A* w = v + D;                        // [D]
+  __shared__ A red[D / 32];
+  const int k = blockIdx.x, bh = blockIdx.y;
+  const size_t to = size_t(level) * G + k;
+  if (t.node_n[to] < 2) return;
+  const int c0 = t.node_chunk0[to], nc = t.node_nchunks[to];
+  for (int e = threadIdx.x; e < D * D; e += blockDim.x) {
+    A s = 0;
+    for (int c = 0; c < nc; ++c) s += pcov[(size_t(bh) * max_chunks + c0 + c) * D * D + e];
+    cov[e] = s;
+  }
+  if (threadIdx.x < D) v[threadIdx.x] = node_v[(size_t(bh) * G + k) * D + threadIdx.x];
+  __syncthreads();
+  for (int it = 0; it < iters; ++it) {
+    if (threadIdx.x < D) {
+      // the covariance is exactly symmetric, so read column i (conflict-free)
+      A s = 0;
+      for (int j = 0; j < D; ++j) s += cov[j * D + threadIdx.x] * v[j];
+      w[threadIdx.x] = s;
+      A sq = s * s;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+      if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sq;
+    }
+    __syncthreads();
+    A nrm2 = 0;
+    for (int i = 0; i < D / 32; ++i) nrm2 += red[i];
+    if (threadIdx.x < D && nrm2 > A(0)) v[threadIdx.x] = w[threadIdx.x] / sqrt(nrm2);
+    __syncthreads();
+  }
+  if (threadIdx.x < D) node_v[(size_t(bh) * G + k) * D + threadIdx.x] = v[threadIdx.x];
+}
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f == 0.f ? 0.f : f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ uint64_t order_key(double f) {
+  uint64_t u = uint64_t(__double_as_longlong(f == 0.0 ? 0.0 : f));
+  return (u >> 63) ? ~u : (u | (uint64_t(1) << 63));
+}
+
+// 4. projection keys, one warp per member
+template <typename T, typename A, int D, typename KeyT>
+__global__ void __launch_bounds__(256) keys_kernel(const T* __restrict__ x, const int32_t* __restrict__ perm, Tables t,
+                                                   int level, int N, int N_pad, int C, int G, const A* node_mu,
+                                                   const A* node_v, KeyT* keys) {
+  __shared__ A mu[D], vv[D];
+  const int c = blockIdx.x, bh = blockIdx.y;
+  const size_t to = size_t(level) * G + c;
+  const int node = t.chunk_node[to], g0 = t.chunk_g0[to], ng = t.chunk_ng[to];
+  if (threadIdx.x < D) {
+    mu[threadIdx.x] = node_mu[(size_t(bh) * G + node) * D + threadIdx.x];
+    vv[threadIdx.x] = node_v[(size_t(bh) * G + node) * D + threadIdx.x];
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const size_t base = size_t(bh) * N_pad + size_t(g0) * C;
+  const T* xb = x + size_t(bh) * N * D;
+  for (int r = warp; r < ng * C; r += 8) {
+    const int tok = perm[base + r];
+    A s = 0;
+    if (tok < N) {
+      for (int dd = lane; dd < D; dd += 32) s += (A(to_f32(xb[size_t(tok) * D + dd])) - mu[dd]) * vv[dd];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) keys[base + r] = tok < N ? order_key(s) : ~KeyT(0);
+  }
+}
+
+// 5. rank split of each node: radix select + stable partition into perm_next
+template <typename KeyT>
+__global__ void __launch_bounds__(1024) split_kernel(const int32_t* __restrict__ perm_cur, int32_t* perm_next,
+                                                     const KeyT* __restrict__ keys, Tables t, int level, int N_pad,
+                                                     int C, int G, uint32_t* status) {
+  __shared__ uint32_t hist[256];
+  __shared__ int warp_tot[32];
+  __shared__ KeyT sh_prefix;
+  __shared__ uint32_t sh_remaining;
+  const int k = blockIdx.x, bh = blockIdx.y;
+  const size_t to = size_t(level) * G + k;
+  const int n = t.node_n[to];
+  if (n < 2) return;
+  const int tid = threadIdx.x;
+  const int len = n * C, m = (n / 2) * C;
+  const size_t base = size_t(bh) * N_pad + size_t(t.node_start[to]) * C;
+  constexpr int kBits = int(sizeof(KeyT)) * 8;
+  KeyT prefix = 0, mask = 0;
+  uint32_t remaining = uint32_t(m);
+  for (int shift = kBits - 8; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < len; i += blockDim.x) {
+      const KeyT key = keys[base + i];
+      if ((key & mask) == prefix) atomicAdd(&hist[uint32_t(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (tid < 32) {
+      uint32_t before;
+      const int b = warp_find_digit(hist, remaining, /*descending=*/false, &before);
+      if (tid == 0) {
+        sh_prefix = prefix | (KeyT(b < 0 ? 0 : b) << shift);
+        sh_remaining = remaining - before;
+      }
+    }
+    __syncthreads();
+    prefix = sh_prefix;
+    remaining = sh_remaining;
+    mask |= KeyT(0xFF) << shift;
+  }
+  const KeyT thr = prefix;
+  const uint32_t need_eq = remaining;
+  int base_left = 0, base_right = 0, base_eq = 0;
+  for (int c0 = 0; c0 < len; c0 += blockDim.x) {
+    const int i = c0 + tid;
+    const bool valid = i < len;
+    const KeyT key = valid ? keys[base + i] : KeyT(0);
+    const int tok = valid ? perm_cur[base + i] : 0;
+    const bool lt = valid && key < thr, eq = valid && key == thr;
+    int eq_tot, left_tot, valid_tot;
+    const int eq_pre = block_excl_count(eq, warp_tot, &eq_tot);
+    const bool left = lt || (eq && uint32_t(base_eq + eq_pre) < need_eq);
+    const int left_pre = block_excl_count(left, warp_tot, &left_tot);
+    const int valid_pre = block_excl_count(valid, warp_tot, &valid_tot);
+    if (valid) {
+      // a correct select gives exactly m left members; stay inside the node regardless
+      const int dst = left ? base_left + left_pre : m + base_right + (valid_pre - left_pre);
+      if (dst < len) perm_next[base + dst] = tok;
+      else raise_status(status, kStatusBounds);
+    }
+    base_left += left_tot;
+    base_right += valid_tot - left_tot;
+    base_eq += eq_tot;
+  }
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t perm_tmp, keys, tables, psum, pcnt, node_mu, node_v, pcov, total;
+  int L, max_chunks;
+};
+
+WsLayout layout(int BH, int N_pad, int C, int G, int d, bool bf16) {
+  WsLayout w{};
+  const size_t asz = bf16 ? sizeof(float) : sizeof(double);
+  w.L = num_levels(G);
+  int mc = 1;
+  for (int l = 0; l < w.L; ++l) mc = std::max(mc, host_level_chunks(G, l));
+  w.max_chunks = mc;
+  size_t off = 0;
+  w.perm_tmp = off; off = align256(off + size_t(BH) * N_pad * 4);
+  w.keys = off; off = align256(off + size_t(BH) * N_pad * 8);
+  w.tables = off; off = align256(off + size_t(7) * std::max(w.L, 1) * G * 4);
+  w.psum = off; off = align256(off + size_t(BH) * mc * d * asz);
+  w.pcnt = off; off = align256(off + size_t(BH) * mc * 4);
+  w.node_mu = off; off = align256(off + size_t(BH) * G * d * asz);
+  w.node_v = off; off = align256(off + size_t(BH) * G * d * asz);
+  w.pcov = off; off = align256(off + size_t(BH) * mc * d * d * asz);
+  w.total = off;
+  return w;
+}
+
+template <typename T, typename A, int D, typename KeyT>
+cudaError_t run_typed(const PddpProblem& p, uint8_t* ws, cudaStream_t s) {
+  const WsLayout w = layout(p.BH, p.N_pad, p.C, p.G, p.d, p.bf16);
+  const int G = p.G;
+  const T* x = static_cast<const T*>(p.q);
+  int32_t* bufs[2];
+  // level l reads bufs[l & 1] and writes bufs[(l + 1) & 1]; the last write lands in p.perm
+  bufs[w.L & 1] = p.perm;
+  bufs[(w.L & 1) ^ 1] = reinterpret_cast<int32_t*>(ws + w.perm_tmp);
+  const size_t total = size_t(p.BH) * p.N_pad;
+  int nlaunch = 0;
+  init_perm_kernel<<<1024, 256, 0, s>>>(bufs[0], p.N_pad, total);
+  ++nlaunch;
+  Tables t;
+  int* tb = reinterpret_cast<int*>(ws + w.tables);
+  const size_t TL = size_t(std::max(w.L, 1)) * G;
+  t.node_start = tb;
+  t.node_n = tb + TL;
+  t.node_chunk0 = tb + 2 * TL;
+  t.node_nchunks = tb + 3 * TL;
+  t.chunk_node = tb + 4 * TL;
+  t.chunk_g0 = tb + 5 * TL;
+  t.chunk_ng = tb + 6 * TL;
+  A* psum = reinterpret_cast<A*>(ws + w.psum);
+  int* pcnt = reinterpret_cast<int*>(ws + w.pcnt);
+  A* node_mu = reinterpret_cast<A*>(ws + w.node_mu);
+  A* node_v = reinterpret_cast<A*>(ws + w.node_v);
+  A* pcov = reinterpret_cast<A*>(ws + w.pcov);
+  KeyT* keys = reinterpret_cast<KeyT*>(ws + w.keys);
+  if (w.L > 0) {
+    tables_kernel<<<w.L, 1024, 0, s>>>(t, G);
+    ++nlaunch;
+  }
+  const int power_smem = int((D * D + 2 * D) * sizeof(A));
+  cudaError_t e = cudaFuncSetAttribute(power_kernel<A, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, power_smem);
+  if (e != cudaSuccess) return e;
+  for (int l = 0; l < w.L; ++l) {
+    const int nodes = 1 << l;
+    const int nch = host_level_chunks(G, l);
+    const dim3 gc(nch, p.BH), gn(nodes, p.BH);
+    int32_t* cur = bufs[l & 1];
+    int32_t* nxt = bufs[(l + 1) & 1];
+    sum_kernel<T, A, D><<<gc, 256, 0, s>>>(x, cur, t, l, p.N, p.N_pad, p.C, G, psum, pcnt, w.max_chunks);
+    mean_kernel<A, D><<<gn, D, 0, s>>>(t, l, G, psum, pcnt, node_mu, node_v, w.max_chunks);
+    cov_kernel<T, A, D><<<gc, 256, 0, s>>>(x, cur, t, l, p.N, p.N_pad, p.C, G, node_mu, pcov, w.max_chunks);
+    power_kernel<A, D><<<gn, 256, power_smem, s>>>(t, l, G, pcov, node_v, p.iters, w.max_chunks);
+    keys_kernel<T, A, D, KeyT><<<gc, 256, 0, s>>>(x, cur, t, l, p.N, p.N_pad, p.C, G, node_mu, node_v, keys);
+    e = cudaMemcpyAsync(nxt, cur, total * sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return e;
+    split_kernel<KeyT><<<gn, 1024, 0, s>>>(cur, nxt, keys, t, l, p.N_pad, p.C, G, p.status);
+    nlaunch += 6;
+  }
+  finalize_kernel<<<1024, 256, 0, s>>>(p.perm, p.group_of, p.N, p.N_pad, p.C, total, p.status);
+  ++nlaunch;
+  note_launches(nlaunch);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t pddp_workspace_bytes(int BH, int N_pad, int C, int G, int d, bool bf16) {
+  return layout(BH, N_pad, C, G, d, bf16).total;
+}
+
+cudaError_t pddp_run(const PddpProblem& p, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  if (p.bf16) {
+    if (p.d == 128) return run_typed<__nv_bfloat16, float, 128, uint32_t>(p, w, stream);
+    if (p.d == 64) return run_typed<__nv_bfloat16, float, 64, uint32_t>(p, w, stream);
+  } else {
+    if (p.d == 128) return run_typed<float, double, 128, uint64_t>(p, w, stream);
+    if (p.d == 64) return run_typed<float, double, 64, uint64_t>(p, w, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mcs

@@ -1,0 +1,200 @@
+"""Thin ctypes binding of libmcs (the C ABI in include/mcs.h).
+
+Functions carry the C names and only marshal arguments: torch tensors become
+device pointers, the current torch CUDA stream becomes the stream argument, and
+a non-OK status raises McsError. Every step of the path runs in libmcs's CUDA
+kernels; there is no fallback. Loading fails loudly when libmcs.so is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from . import build as _build
+
+MCS_OK = 0
+STATUS_NAMES = {0: "MCS_OK", 1: "MCS_ERR_INVALID_ARG", 2: "MCS_ERR_UNSUPPORTED", 3: "MCS_ERR_WORKSPACE",
+                4: "MCS_ERR_CUDA", 5: "MCS_ERR_DEVICE_BOUNDS", 6: "MCS_ERR_DEVICE_TIMEOUT"}
+MCS_F32, MCS_BF16 = 0, 1
+
+EXPORTS = ("mcs_workspace_size", "mcs_group_pddp", "mcs_dense_attn", "mcs_anchor_select",
+           "mcs_sparse_attn_gather", "mcs_anchor_residual", "mcs_residual_store", "mcs_residual_apply",
+           "mcs_check_status", "mcs_status_string", "mcs_launch_count", "mcs_selftest_tc_mma")
+
+
+class McsError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(code, code)} ({_status_string(code)})")
+
+
+class mcs_desc(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("N", ctypes.c_int), ("d", ctypes.c_int),
+                ("C", ctypes.c_int), ("dtype", ctypes.c_int), ("scale", ctypes.c_float),
+                ("pddp_iters", ctypes.c_int)]
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """Load libmcs.so (optionally building it first) and declare the signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        if not build_if_missing:
+            raise RuntimeError(f"libmcs.so not built at {_build.LIB}: run sparse_attention_diffusion_gb300.build.build()")
+        _build.build()
+    L = ctypes.CDLL(_build.LIB)
+    P, I, Z, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+    D = ctypes.POINTER(mcs_desc)
+    sig = {
+        "mcs_workspace_size": (Z, [D, I]),
+        "mcs_group_pddp": (I, [D, P, P, P, P, Z, S]),
+        "mcs_dense_attn": (I, [D, P, P, P, P, P, S]),
+        "mcs_anchor_select": (I, [D, P, P, P, P, I, P, P, P, Z, S]),
+        "mcs_sparse_attn_gather": (I, [D, P, P, P, P, P, I, P, P, S]),
+        "mcs_anchor_residual": (I, [D, P, P, P, P, P, I, P, P, S]),
+        "mcs_residual_store": (I, [D, P, P, P, S]),
+        "mcs_residual_apply": (I, [D, P, P, P, S]),
+        "mcs_check_status": (I, [S]),
+        "mcs_status_string": (ctypes.c_char_p, [I]),
+        "mcs_launch_count": (ctypes.c_uint64, []),
+        "mcs_selftest_tc_mma": (I, [P, P, P, I, ctypes.c_uint32, ctypes.c_uint32, S]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype, fn.argtypes = res, args
+    _lib = L
+    return L
+
+
+def _status_string(code) -> str:
+    try:
+        return load().mcs_status_string(code).decode()
+    except Exception:
+        return "?"
+
+
+def _check(fn, code):
+    if code != MCS_OK:
+        raise McsError(fn, code)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libmcs takes device tensors")
+    if not t.is_contiguous():
+        raise ValueError("libmcs takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def make_desc(B, H, N, d, C, dtype, scale=0.0, pddp_iters=20) -> mcs_desc:
+    dt = MCS_BF16 if dtype in (torch.bfloat16, "bf16", MCS_BF16) else MCS_F32
+    return mcs_desc(B, H, N, d, C, dt, float(scale), int(pddp_iters))
+
+
+def desc_for(x: torch.Tensor, C: int, pddp_iters: int = 20) -> mcs_desc:
+    B, H, N, d = x.shape
+    return make_desc(B, H, N, d, C, x.dtype, 0.0, pddp_iters)
+
+
+def geometry(desc: mcs_desc):
+    G = -(-desc.N // desc.C)
+    return G, G * desc.C
+
+
+def mcs_workspace_size(desc: mcs_desc, K: int = 1) -> int:
+    return int(load().mcs_workspace_size(ctypes.byref(desc), int(K)))
+
+
+def workspace(desc: mcs_desc, K: int = 1, device="cuda") -> torch.Tensor:
+    n = mcs_workspace_size(desc, K)
+    if n == 0:
+        raise McsError("mcs_workspace_size", 2)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def mcs_group_pddp(desc, q, perm, group_of, ws, stream=None):
+    _check("mcs_group_pddp", load().mcs_group_pddp(ctypes.byref(desc), _ptr(q), _ptr(perm), _ptr(group_of), _ptr(ws),
+                                                   ws.numel(), _stream(stream)))
+
+
+def mcs_dense_attn(desc, q, k, v, o, lse, stream=None):
+    _check("mcs_dense_attn", load().mcs_dense_attn(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                                   _stream(stream)))
+
+
+def mcs_anchor_select(desc, q, k, perm, lse, K, idx, mass, ws, stream=None):
+    _check("mcs_anchor_select", load().mcs_anchor_select(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(perm), _ptr(lse),
+                                                         int(K), _ptr(idx), _ptr(mass), _ptr(ws), ws.numel(),
+                                                         _stream(stream)))
+
+
+def mcs_sparse_attn_gather(desc, q, k, v, perm, idx, K, residual, o, stream=None):
+    _check("mcs_sparse_attn_gather", load().mcs_sparse_attn_gather(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v),
+                                                                   _ptr(perm), _ptr(idx), int(K), _ptr(residual),
+                                                                   _ptr(o), _stream(stream)))
+
+
+def mcs_anchor_residual(desc, q, k, v, perm, idx, K, o_dense, r, stream=None):
+    _check("mcs_anchor_residual", load().mcs_anchor_residual(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(perm),
+                                                             _ptr(idx), int(K), _ptr(o_dense), _ptr(r),
+                                                             _stream(stream)))
+
+
+def mcs_residual_store(desc, o_dense, o_sparse, r, stream=None):
+    _check("mcs_residual_store", load().mcs_residual_store(ctypes.byref(desc), _ptr(o_dense), _ptr(o_sparse), _ptr(r),
+                                                           _stream(stream)))
+
+
+def mcs_residual_apply(desc, o_sparse, r, o, stream=None):
+    _check("mcs_residual_apply", load().mcs_residual_apply(ctypes.byref(desc), _ptr(o_sparse), _ptr(r), _ptr(o),
+                                                           _stream(stream)))
+
+
+def mcs_check_status(stream=None):
+    _check("mcs_check_status", load().mcs_check_status(_stream(stream)))
+
+
+def mcs_launch_count() -> int:
+    return int(load().mcs_launch_count())
+
+
+def mcs_selftest_tc_mma(a, b, d, mode, mn_lbo=16384, mn_sbo=1024, stream=None):
+    _check("mcs_selftest_tc_mma", load().mcs_selftest_tc_mma(_ptr(a), _ptr(b), _ptr(d), int(mode), int(mn_lbo),
+                                                             int(mn_sbo), _stream(stream)))
+
+
+# ---------------------------------------------------------------- convenience: buffers for one layer
+def alloc_cache(desc: mcs_desc, K: int, dtype, device="cuda"):
+    """Caller-owned meta-cache buffers {perm, group_of, idx, mass, residual} for one layer."""
+    G, N_pad = geometry(desc)
+    BH = desc.B * desc.H
+    return dict(
+        perm=torch.empty((desc.B, desc.H, N_pad), dtype=torch.int32, device=device),
+        group_of=torch.empty((desc.B, desc.H, desc.N), dtype=torch.int32, device=device),
+        idx=torch.empty((desc.B, desc.H, G, K), dtype=torch.int32, device=device),
+        mass=torch.empty((desc.B, desc.H, G), dtype=torch.float32, device=device),
+        residual=torch.empty((desc.B, desc.H, desc.N, desc.d), dtype=dtype, device=device),
+    )
+
+
+def density_K(density, N) -> int:
+    from fractions import Fraction
+    return int(math.ceil(Fraction(str(density)) * N))

@@ -1,0 +1,41 @@
+"""tcgen05 descriptor self-test: one MMA chain through the C ABI against a float64
+matmul of the same bf16 operands (K-major and MN-major B operands)."""
+import pytest
+import torch
+
+from sparse_attention_diffusion_gb300 import mcs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    mcs.load(build_if_missing=True)
+    return torch.device("cuda")
+
+
+def _operands(seed, dev):
+    g = torch.Generator().manual_seed(seed)
+    a = torch.randn(128, 64, generator=g).to(torch.bfloat16)
+    b = torch.randn(128, 64, generator=g).to(torch.bfloat16)
+    return a, b
+
+
+def test_kmajor_b(dev):
+    a, b = _operands(0, dev)
+    d = torch.zeros(128, 128, dtype=torch.float32, device=dev)
+    mcs.mcs_selftest_tc_mma(a.to(dev), b.to(dev), d, 0)
+    mcs.mcs_check_status()
+    ref = a.double() @ b.double().T
+    assert torch.allclose(d.cpu().double(), ref, atol=1e-3, rtol=1e-4)
+
+
+def test_mnmajor_b(dev):
+    a, b = _operands(1, dev)
+    bt = b.T.contiguous()                   # [64 (K) x 128 (N)], N contiguous
+    d = torch.zeros(128, 128, dtype=torch.float32, device=dev)
+    mcs.mcs_selftest_tc_mma(a.to(dev), bt.to(dev), d, 1, 16384, 1024)
+    mcs.mcs_check_status()
+    ref = a.double() @ bt.double()
+    assert torch.allclose(d.cpu().double(), ref, atol=1e-3, rtol=1e-4)
