@@ -151,10 +151,18 @@ uint64_t mcs_launch_count(void);
  * descriptor encodings the attention kernels rely on. a: bf16 [128 x 64]
  * row-major; mode 0: b is bf16 [128 x 64] row-major (K-major operand,
  * D = A B^T); mode 1: b is bf16 [64 x 128] row-major (MN-major operand, D = A B)
- * with the descriptor's leading/stride byte offsets mn_lbo / mn_sbo. d: fp32
- * [128 x 128] output. All device pointers. */
+ * with the descriptor's leading/stride byte offsets mn_lbo / mn_sbo; mode 2: as
+ * mode 0 with A read from tensor memory. d: fp32 [128 x 128] output. All device
+ * pointers. */
 mcs_status mcs_selftest_tc_mma(const void *a, const void *b, float *d, int mode, uint32_t mn_lbo, uint32_t mn_sbo,
                                mcs_stream stream);
+
+/* Diagnostic (no counterpart in the method): gathers 128 rows of the bf16 matrix
+ * src [nrows x 128] (row-major, device) with TMA 4-row gathers into the swizzled
+ * shared-memory layout of the attention kernels and writes them back row-major:
+ * out[i, :] = src[rows[i], :], zeros where rows[i] >= nrows. rows: int32 [128]
+ * device; out: bf16 [128 x 128] device. */
+mcs_status mcs_selftest_tma_gather(const void *src, int nrows, const int32_t *rows, void *out, mcs_stream stream);
 
 #ifdef __cplusplus
 }

@@ -383,11 +383,19 @@ uint64_t mcs_launch_count(void) { return g_launches.load(std::memory_order_relax
 
 mcs_status mcs_selftest_tc_mma(const void* a, const void* b, float* d, int mode, uint32_t mn_lbo, uint32_t mn_sbo,
                                mcs_stream stream) {
-  if (!aligned16(a) || !aligned16(b) || !aligned16(d) || (mode != 0 && mode != 1)) return MCS_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(d) || mode < 0 || mode > 2) return MCS_ERR_INVALID_ARG;
   uint32_t* status = nullptr;
   mcs_status st = device_state(&status, nullptr);
   if (st != MCS_OK) return st;
   return from_cuda(mcs::tc_probe(a, b, d, mode, mn_lbo, mn_sbo, status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mcs_status mcs_selftest_tma_gather(const void* src, int nrows, const int32_t* rows, void* out, mcs_stream stream) {
+  if (!aligned16(src) || !aligned16(rows) || !aligned16(out) || nrows < 1) return MCS_ERR_INVALID_ARG;
+  uint32_t* status = nullptr;
+  mcs_status st = device_state(&status, nullptr);
+  if (st != MCS_OK) return st;
+  return from_cuda(mcs::tma_gather_probe(src, nrows, rows, out, status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -37,6 +37,8 @@ struct TcColsumParams {
 cudaError_t tc_dense_attn(int D, const TcAttnParams& p, int BH, bool with_pv, cudaStream_t stream);
 cudaError_t tc_sparse_attn(int D, int epi, const TcAttnParams& p, int BH, cudaStream_t stream);
 cudaError_t tc_colsum(int D, int C, const TcColsumParams& p, int nrows, cudaStream_t stream);
+cudaError_t tma_gather_probe(const void* src, int nrows, const int* rows, void* out, uint32_t* status,
+                             cudaStream_t stream);
 cudaError_t tc_probe(const void* a, const void* b, float* d, int mode, uint32_t lbo, uint32_t sbo, uint32_t* status,
                      cudaStream_t stream);
 

@@ -22,7 +22,8 @@ MCS_F32, MCS_BF16 = 0, 1
 
 EXPORTS = ("mcs_workspace_size", "mcs_group_pddp", "mcs_dense_attn", "mcs_anchor_select",
            "mcs_sparse_attn_gather", "mcs_anchor_residual", "mcs_residual_store", "mcs_residual_apply",
-           "mcs_check_status", "mcs_status_string", "mcs_launch_count", "mcs_selftest_tc_mma")
+           "mcs_check_status", "mcs_status_string", "mcs_launch_count", "mcs_selftest_tc_mma",
+           "mcs_selftest_tma_gather")
 
 
 class McsError(RuntimeError):
@@ -69,6 +70,7 @@ def load(build_if_missing: bool = False):
         "mcs_status_string": (ctypes.c_char_p, [I]),
         "mcs_launch_count": (ctypes.c_uint64, []),
         "mcs_selftest_tc_mma": (I, [P, P, P, I, ctypes.c_uint32, ctypes.c_uint32, S]),
+        "mcs_selftest_tma_gather": (I, [P, I, P, P, S]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -179,6 +181,11 @@ def mcs_launch_count() -> int:
 def mcs_selftest_tc_mma(a, b, d, mode, mn_lbo=16384, mn_sbo=1024, stream=None):
     _check("mcs_selftest_tc_mma", load().mcs_selftest_tc_mma(_ptr(a), _ptr(b), _ptr(d), int(mode), int(mn_lbo),
                                                              int(mn_sbo), _stream(stream)))
+
+
+def mcs_selftest_tma_gather(src, rows, out, stream=None):
+    _check("mcs_selftest_tma_gather", load().mcs_selftest_tma_gather(_ptr(src), int(src.shape[0]), _ptr(rows), _ptr(out),
+                                                                     _stream(stream)))
 
 
 # ---------------------------------------------------------------- convenience: buffers for one layer

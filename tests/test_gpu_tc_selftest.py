@@ -39,3 +39,27 @@ def test_mnmajor_b(dev):
     mcs.mcs_check_status()
     ref = a.double() @ bt.double()
     assert torch.allclose(d.cpu().double(), ref, atol=1e-3, rtol=1e-4)
+
+
+def test_a_operand_from_tensor_memory(dev):
+    a, b = _operands(2, dev)
+    d = torch.zeros(128, 128, dtype=torch.float32, device=dev)
+    mcs.mcs_selftest_tc_mma(a.to(dev), b.to(dev), d, 2)
+    mcs.mcs_check_status()
+    ref = a.double() @ b.double().T
+    assert torch.allclose(d.cpu().double(), ref, atol=1e-3, rtol=1e-4)
+
+
+def test_tma_gather4_rows(dev):
+    g = torch.Generator().manual_seed(3)
+    src = torch.randn(1000, 128, generator=g).to(torch.bfloat16)
+    rows = torch.randint(0, 1000, (128,), generator=g, dtype=torch.int32)
+    rows[5] = 1000          # out of range -> zeros
+    rows[77] = 5000
+    out = torch.empty(128, 128, dtype=torch.bfloat16, device=dev)
+    mcs.mcs_selftest_tma_gather(src.to(dev), rows.to(dev), out)
+    mcs.mcs_check_status()
+    want = torch.zeros(128, 128, dtype=torch.bfloat16)
+    ok = rows < 1000
+    want[ok] = src[rows[ok].long()]
+    assert torch.equal(out.cpu(), want)
