@@ -94,6 +94,7 @@ mcs_status dense_impl(const Dims& dm, const void* q, const void* k, const void* 
     p.v = static_cast<const __nv_bfloat16*>(v);
     p.o = static_cast<__nv_bfloat16*>(o);
     p.lse = lse;
+    p.BH = dm.BH;
     p.N = dm.N;
     p.N_pad = dm.N_pad;
     p.C = dm.C;
@@ -134,6 +135,7 @@ mcs_status sparse_impl(const Dims& dm, int epi, const void* q, const void* k, co
     p.idx = idx;
     p.res_in = static_cast<const __nv_bfloat16*>(res_in);
     p.res_out = static_cast<__nv_bfloat16*>(res_out);
+    p.BH = dm.BH;
     p.N = dm.N;
     p.N_pad = dm.N_pad;
     p.C = dm.C;

@@ -1,21 +1,14 @@
 // tcgen05 (5th-generation tensor core) attention kernels for bf16 inputs on sm_103a.
 //
-//  * attn_tc_kernel: one CTA computes softmax attention for one tile of 128
-//    query rows. Dense mode walks every key of the head in tiles of 128;
-//    sparse mode gathers the group's queries through perm and walks the group's
-//    K selected keys, fetched row by row from the index list (keys are gathered,
-//    not repacked into blocks) [MC-Sparse summary: index-gather / PDDP paragraph].
-//    S = Q K^T and O += P V run on the tensor core with fp32 accumulators in
-//    tensor memory; the softmax (online, base-2, lazily rescaled) runs on the
-//    CUDA cores, one thread per query row.
 //  * colsum_tc_kernel: pass 2 of the anchor selection. For one query group it
 //    forms the transposed logits S^T = K_tile Q_g^T (the key on the TMEM lane),
 //    so each thread owns one key and sums exp(s - lse) over the group's queries
 //    without cross-thread reduction [MC-Sparse summary: anchor two-pass paragraph].
+//  * self-test kernels for the descriptor encodings and the TMA gathers.
 //
-// Warp roles (288 threads): warps 0-3 softmax / column sums (thread = TMEM lane),
-// warp 4 tensor-memory allocation and the single MMA-issuing thread, warps 5-8
-// producers (cp.async row gathers into 128-byte-swizzled shared memory).
+// Warp roles of colsum_tc_kernel (288 threads): warps 0-3 column sums (thread =
+// TMEM lane = key), warp 4 tensor-memory allocation and the single MMA-issuing
+// thread, warps 5-8 producers (cp.async into 128-byte-swizzled shared memory).
 // Every wait is bounded; on a timeout the CTA raises a status flag, drains its
 // in-flight copies and MMAs, frees tensor memory and returns.
 #include <cstdio>
@@ -23,370 +16,13 @@
 #include "attn_tc.h"
 #include "common.cuh"
 #include "ptx.cuh"
+#include "tc_common.cuh"
 #include "tma.cuh"
 
 namespace mcs {
 namespace {
 
 constexpr int kThreads = 288;
-constexpr int kRegion = 128 * 128;  // one 128-byte-swizzled region: 128 rows x 128 B
-
-// Byte offset of the 16-byte chunk `ch` (8 bf16 along the contiguous dim) of row
-// `row` inside a [rows x 64*nregions] tile stored as 128B-swizzled regions.
-__device__ __forceinline__ uint32_t sw128_off(int row, int ch) {
-  return uint32_t((ch >> 3) * kRegion + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
-}
-
-// K-major operand (rows = M or N, contiguous dim = K): k-step s covers K elements
-// [16s, 16s+16): region s/4, +32 B per step inside the 128-byte swizzle atom.
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int s) {
-  return smem_desc_sw128(base + uint32_t((s >> 2) * kRegion + (s & 3) * 32), 16, 1024);
-}
-// MN-major operand (contiguous dim = N, rows = K): k-step s covers rows [16s, 16s+16).
-// Leading byte offset = stride between 64-element N chunks (one region),
-// stride byte offset = stride between groups of 8 rows.
-__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int s) {
-  return smem_desc_sw128(base + uint32_t(s * 16 * 128), kRegion, 1024);
-}
-
-__device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
-
-template <int D>
-struct AttnSmem {
-  static constexpr int kTile = (D / 64) * kRegion;   // [128 x D] bf16
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTile;              // 2 stages
-  static constexpr int kV = kK + 2 * kTile;          // 2 stages
-  static constexpr int kP = kV + 2 * kTile;          // [128 x 128] bf16
-  static constexpr int kBar = kP + 2 * kRegion;
-  static constexpr int kNumBars = 18;
-  static constexpr int kMisc = kBar + kNumBars * 8;  // tmem slot, abort flag
-  static constexpr int kTok = kMisc + 16;            // q tokens [128], k tokens [2][128], v tokens [2][128]
-  static constexpr int kBytes = kTok + 5 * 128 * 4;
-  static constexpr int kAlloc = kBytes + 1024;
-};
-
-template <int D, bool kSparse, int kEpi, bool kPV>
-__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const TcAttnParams p) {
-  using L = AttnSmem<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sbase = smem_u32(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;   // [2]
-  uint64_t* k_empty = bars + 3;  // [2]
-  uint64_t* v_full = bars + 5;   // [2]
-  uint64_t* v_empty = bars + 7;  // [2]
-  uint64_t* s_full = bars + 9;   // [2]
-  uint64_t* s_free = bars + 11;  // [2]
-  uint64_t* p_full = bars + 13;
-  uint64_t* p_empty = bars + 14;
-  uint64_t* o_done = bars + 15;
-  uint64_t* drain = bars + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
-  int32_t* q_tok = reinterpret_cast<int32_t*>(smem + L::kTok);
-  int32_t* k_tok = q_tok + 128;
-  int32_t* v_tok = q_tok + 384;
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.y, tile = blockIdx.x;
-  const int nkv = kSparse ? p.K : p.N;
-  const int T = (nkv + 127) / 128;
-  uint32_t* st = p.status;
-
-  if (tid == 0) {
-    mbar_init(q_full, 128);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(k_full + s, 64);
-      mbar_init(k_empty + s, 1);
-      mbar_init(v_full + s, 64);
-      mbar_init(v_empty + s, 1);
-      mbar_init(s_full + s, 1);
-      mbar_init(s_free + s, 128);
-    }
-    mbar_init(p_full, 128);
-    mbar_init(p_empty, 1);
-    mbar_init(o_done, 1);
-    mbar_init(drain, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 4) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem;          // two S buffers: columns [0,128) and [128,256)
-  const uint32_t tO = tmem + 256;    // O accumulator: columns [256, 256+D)
-
-  if (warp >= 5) {
-    // ------------------------------------------------------------ producers
-    const int pt = tid - 160;  // 0..127
-    // Q tile: row r holds token q_tok[r] (or zeros).
-    {
-      int tok = -1;
-      if constexpr (kSparse) {
-        if (pt < p.C) {
-          const int t = p.perm[size_t(bh) * p.N_pad + size_t(tile) * p.C + pt];
-          if (t < 0 || t >= p.N_pad) raise_status(st, kStatusBounds);
-          else if (t < p.N) tok = t;
-        }
-      } else {
-        const int t = tile * 128 + pt;
-        if (t < p.N) tok = t;
-      }
-      q_tok[pt] = tok;
-      named_bar_sync(1, 128);
-      const __nv_bfloat16* qb = p.q + size_t(bh) * p.N * D;
-#pragma unroll 4
-      for (int it = 0; it < D / 8; ++it) {
-        const int id = it * 128 + pt, row = id / (D / 8), ch = id % (D / 8);
-        const int t = q_tok[row];
-        cp_async16(sbase + L::kQ + sw128_off(row, ch), qb + size_t(t < 0 ? 0 : t) * D + ch * 8, t >= 0);
-      }
-      cp_async_commit();
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      mbar_arrive(q_full);
-    }
-    // K (threads 0-63) and V (threads 64-127) pipelines.
-    const bool isK = pt < 64;
-    const int gt = pt & 63;
-    if (isK || kPV) {
-      uint64_t* full = isK ? k_full : v_full;
-      uint64_t* empty = isK ? k_empty : v_empty;
-      int32_t* toks = isK ? k_tok : v_tok;
-      const __nv_bfloat16* src = (isK ? p.k : p.v) + size_t(bh) * p.N * D;
-      const uint32_t sm = sbase + (isK ? L::kK : L::kV);
-      const uint32_t bar_id = isK ? 2 : 3;
-      const int32_t* idxg = kSparse ? p.idx + (size_t(bh) * p.G + tile) * size_t(p.K) : nullptr;
-      volatile int* grp_stop = abort_flag + (isK ? 1 : 2);  // written by the group leader only
-      int j = 0;
-      for (; j < T; ++j) {
-        const int s = j & 1;
-        const uint32_t u = uint32_t(j) >> 1;
-        if (gt == 0) {
-          int stop = *abort_flag;
-          if (!stop && !mbar_wait(empty + s, (u & 1) ^ 1, st)) {
-            raise_status(st, kStatusTimeout);
-            *abort_flag = 1;
-            stop = 1;
-          }
-          *grp_stop = stop;
-        }
-        named_bar_sync(bar_id, 64);
-        if (*grp_stop) break;
-        for (int r = gt; r < 128; r += 64) {
-          const int slot = j * 128 + r;
-          int tok = -1;
-          if (slot < nkv) {
-            const int t = kSparse ? idxg[slot] : slot;
-            if (t < 0 || t >= p.N) raise_status(st, kStatusBounds);
-            else tok = t;
-          }
-          toks[s * 128 + r] = tok;
-        }
-        named_bar_sync(bar_id, 64);
-#pragma unroll 4
-        for (int it = 0; it < 2 * D / 8; ++it) {
-          const int id = it * 64 + gt, row = id / (D / 8), ch = id % (D / 8);
-          const int t = toks[s * 128 + row];
-          cp_async16(sm + s * L::kTile + sw128_off(row, ch), src + size_t(t < 0 ? 0 : t) * D + ch * 8, t >= 0);
-        }
-        cp_async_commit();
-        if (j >= 1) {
-          cp_async_wait<1>();
-          fence_proxy_async_smem();
-          mbar_arrive(full + ((j - 1) & 1));
-        }
-      }
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      if (j == T && T > 0) mbar_arrive(full + ((T - 1) & 1));
-    }
-  } else if (warp == 4) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
-      bool ok = mbar_wait(q_full, 0, st);
-      bool issued = false;
-      auto issue_pv = [&](int i) -> bool {
-        const int s = i & 1;
-        const uint32_t u = uint32_t(i) >> 1;
-        if (!mbar_wait(v_full + s, u & 1, st)) return false;
-        if (!mbar_wait(p_full, uint32_t(i) & 1, st)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          tc_mma_ss(tO, desc_kmajor(sbase + L::kP, ks), desc_mnmajor(sbase + L::kV + s * L::kTile, ks), kIdescPV,
-                    (i > 0 || ks > 0) ? 1u : 0u);
-        tc_commit(p_empty);
-        tc_commit(v_empty + s);
-        return true;
-      };
-      for (int j = 0; ok && j < T; ++j) {
-        const int s = j & 1;
-        const uint32_t u = uint32_t(j) >> 1;
-        ok = mbar_wait(k_full + s, u & 1, st) && mbar_wait(s_free + s, (u & 1) ^ 1, st);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          tc_mma_ss(tS + s * 128, desc_kmajor(sbase + L::kQ, ks), desc_kmajor(sbase + L::kK + s * L::kTile, ks),
-                    kIdescQK, ks > 0 ? 1u : 0u);
-        tc_commit(s_full + s);
-        tc_commit(k_empty + s);
-        issued = true;
-        if (kPV && j >= 1) ok = issue_pv(j - 1);
-      }
-      if (ok && kPV && T > 0) ok = issue_pv(T - 1);
-      if (ok) tc_commit(o_done);
-      if (!ok) {
-        raise_status(st, kStatusTimeout);
-        *abort_flag = 1;
-        if (issued) {
-          tc_commit(drain);
-          mbar_wait(drain, 0, st);
-        }
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ softmax (thread = query row)
-    const int row = tid;
-    const uint32_t lane_off = uint32_t(warp * 32) << 16;
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    uint8_t* sP = smem + L::kP;
-    for (int j = 0; j < T; ++j) {
-      const int b = j & 1;
-      const uint32_t u = uint32_t(j) >> 1;
-      ok = warp_all(mbar_wait(s_full + b, u & 1, st));
-      if (!ok) break;
-      tc_fence_after();
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tS + lane_off + b * 128 + c * 32, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
-      }
-      tc_fence_before();
-      mbar_arrive(s_free + b);
-      const int nvalid = min(128, nkv - j * 128);
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 128; ++c) mx = fmaxf(mx, c < nvalid ? s[c] : -INFINITY);
-      const float m_new = fmaxf(m, mx * p.scale_log2);
-      const bool need = m_new > m + 8.f;  // lazy rescale: keep a stale max unless it grew by > 2^8
-      if constexpr (kPV) {
-        ok = warp_all(mbar_wait(p_empty, (uint32_t(j) & 1) ^ 1, st));  // PV of tile j-1 done
-        if (!ok) break;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, need && j > 0)) {
-          const float alpha = (need && j > 0) ? ex2_approx(m - m_new) : 1.f;
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tO + lane_off + c * 32, r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st32(tO + lane_off + c * 32, r);
-          }
-        }
-      }
-      if (need) {
-        l *= ex2_approx(m - m_new);
-        m = m_new;
-      }
-      const float neg_m = -m;
-#pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        s[c] = c < nvalid ? ex2_approx(fmaf(s[c], p.scale_log2, neg_m)) : 0.f;
-        l += s[c];
-      }
-      if constexpr (kPV) {
-#pragma unroll
-        for (int c8 = 0; c8 < 16; ++c8) {
-          uint4 v;
-          v.x = pack_bf16x2(s[c8 * 8 + 0], s[c8 * 8 + 1]);
-          v.y = pack_bf16x2(s[c8 * 8 + 2], s[c8 * 8 + 3]);
-          v.z = pack_bf16x2(s[c8 * 8 + 4], s[c8 * 8 + 5]);
-          v.w = pack_bf16x2(s[c8 * 8 + 6], s[c8 * 8 + 7]);
-          *reinterpret_cast<uint4*>(sP + sw128_off(row, c8)) = v;
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(p_full);
-      }
-    }
-    // ------------------------------------------------------------ epilogue
-    int tok = -1;
-    if constexpr (kSparse) {
-      if (row < p.C) {
-        const int t = p.perm[size_t(bh) * p.N_pad + size_t(tile) * p.C + row];
-        if (t >= 0 && t < p.N) tok = t;
-      }
-    } else {
-      const int t = tile * 128 + row;
-      if (t < p.N) tok = t;
-    }
-    if (ok && !kSparse && p.lse != nullptr && tok >= 0)
-      p.lse[size_t(bh) * p.N + tok] = (m + __log2f(l)) * kLn2;
-    if constexpr (kPV) {
-      if (ok) ok = warp_all(mbar_wait(o_done, 0, st));
-      if (ok) {
-        tc_fence_after();
-        const float inv_l = 1.f / l;
-        const size_t rowoff = (size_t(bh) * p.N + size_t(tok < 0 ? 0 : tok)) * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tO + lane_off + c * 32, r);
-          if (tok >= 0 && (kEpi == kEpiStoreResidual || p.o != nullptr)) {
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              float o8[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) o8[i] = __uint_as_float(r[q4 * 8 + i]) * inv_l;
-              const size_t off = rowoff + c * 32 + q4 * 8;
-              if constexpr (kEpi != kEpiPlain) {
-                const uint4 rv = *reinterpret_cast<const uint4*>(p.res_in + off);
-                const __nv_bfloat16* rb = reinterpret_cast<const __nv_bfloat16*>(&rv);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  o8[i] = (kEpi == kEpiAddResidual) ? o8[i] + __bfloat162float(rb[i]) : __bfloat162float(rb[i]) - o8[i];
-              }
-              uint4 w;
-              w.x = pack_bf16x2(o8[0], o8[1]);
-              w.y = pack_bf16x2(o8[2], o8[3]);
-              w.z = pack_bf16x2(o8[4], o8[5]);
-              w.w = pack_bf16x2(o8[6], o8[7]);
-              __nv_bfloat16* dst = (kEpi == kEpiStoreResidual) ? p.res_out : p.o;
-              *reinterpret_cast<uint4*>(dst + off) = w;
-            }
-          }
-        }
-      }
-    }
-    if (!ok) {
-      raise_status(st, kStatusTimeout);
-      *abort_flag = 1;
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 4) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
 
 // ---------------------------------------------------------------- select pass 2
 template <int D, int CQ>
@@ -715,39 +351,6 @@ cudaError_t set_smem(K kernel, int bytes) {
 }  // namespace
 
 // ---------------------------------------------------------------- host launchers
-template <int D, bool kSparse, int kEpi, bool kPV>
-static cudaError_t launch_attn(const TcAttnParams& p, int BH, cudaStream_t stream) {
-  using L = AttnSmem<D>;
-  auto kern = attn_tc_kernel<D, kSparse, kEpi, kPV>;
-  cudaError_t e = set_smem(kern, L::kAlloc);
-  if (e != cudaSuccess) return e;
-  dim3 grid(p.tiles_per_head, BH);
-  kern<<<grid, kThreads, L::kAlloc, stream>>>(p);
-  note_launches(1);
-  return cudaGetLastError();
-}
-
-cudaError_t tc_dense_attn(int D, const TcAttnParams& p, int BH, bool with_pv, cudaStream_t stream) {
-  if (D == 128) return with_pv ? launch_attn<128, false, kEpiPlain, true>(p, BH, stream)
-                               : launch_attn<128, false, kEpiPlain, false>(p, BH, stream);
-  if (D == 64) return with_pv ? launch_attn<64, false, kEpiPlain, true>(p, BH, stream)
-                              : launch_attn<64, false, kEpiPlain, false>(p, BH, stream);
-  return cudaErrorInvalidValue;
-}
-
-cudaError_t tc_sparse_attn(int D, int epi, const TcAttnParams& p, int BH, cudaStream_t stream) {
-#define MCS_SPARSE_CASE(DD, EE) \
-  if (D == DD && epi == EE) return launch_attn<DD, true, EE, true>(p, BH, stream);
-  MCS_SPARSE_CASE(128, kEpiPlain)
-  MCS_SPARSE_CASE(128, kEpiAddResidual)
-  MCS_SPARSE_CASE(128, kEpiStoreResidual)
-  MCS_SPARSE_CASE(64, kEpiPlain)
-  MCS_SPARSE_CASE(64, kEpiAddResidual)
-  MCS_SPARSE_CASE(64, kEpiStoreResidual)
-#undef MCS_SPARSE_CASE
-  return cudaErrorInvalidValue;
-}
-
 template <int D, int CQ>
 static cudaError_t launch_colsum(const TcColsumParams& p, int nrows, cudaStream_t stream) {
   using L = ColsumSmem<D, CQ>;

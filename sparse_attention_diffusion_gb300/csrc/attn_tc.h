@@ -16,7 +16,7 @@ struct TcAttnParams {
   const int32_t* idx;           // sparse: [BH, G, K]
   const __nv_bfloat16* res_in;  // add-residual: R; store-residual: o_dense
   __nv_bfloat16* res_out;       // store-residual: R
-  int N, N_pad, C, G, K;
+  int BH, N, N_pad, C, G, K;
   int tiles_per_head;           // dense: ceil(N/128) query tiles; sparse: G groups
   float scale_log2;             // scale * log2(e)
   uint32_t* status;
