@@ -5,11 +5,15 @@
 // [MC-Sparse summary: index-gather / PDDP paragraph; residual paragraph].
 //
 // One CTA owns one tile of 128 query rows (dense: rows 128t..128t+127; sparse:
-// the C members of group t, read through perm). 192 threads:
-//   warp 5      TMA producer: Q tile, then a 3-stage ring of K and V tiles of
-//               128 keys. Dense tiles are tiled TMA boxes; sparse tiles are built
-//               from 4-row TMA gathers (tile::gather4) at the group's key indices,
-//               so no thread ever waits on a copy. K runs one tile ahead of V.
+// the C members of group t, read through perm). K and V arrive in a 3-stage
+// ring of tiles of 128 keys:
+//   dense:  warp 5 is a TMA producer loading tiled boxes (Q once, then K_i ahead
+//           of V_{i-1}); no thread waits on a copy.
+//   sparse: warps 4-11 gather the rows with 16-byte cp.async copies at the group's
+//           key indices (streamed through a shared-memory index ring) and signal
+//           each tile two tiles after issuing it. Row gathers of 128-byte
+//           segments are kept on the load/store path: on this GPU they move far
+//           more bytes per cycle than 4-row TMA gathers.
 //   warp 4      tensor-memory allocation and the single MMA-issuing thread:
 //               S_j = Q K_j^T into one of two TMEM S buffers, then O += P_{j-1} V_{j-1}
 //               with P read from tensor memory (A operand) and V from shared memory.
@@ -29,7 +33,19 @@
 namespace mcs {
 namespace {
 
-constexpr int kFwdThreads = 192;
+// dense (192 threads): warps 0-3 softmax, warp 4 MMA, warp 5 TMA producer.
+// sparse (512 threads, four warpgroups): warpgroup 0 softmax, warpgroups 1-2
+// eight cp.async gather warps, warpgroup 3 the MMA warp (warp 12) and three idle
+// warps. Row gathers need many warps in flight, so the registers are rebalanced
+// with setmaxnreg: softmax up, gather and MMA down. The split below must fit in
+// the 512 x (launch registers) the block starts with, which the launcher checks.
+template <bool kSparse>
+__host__ __device__ constexpr int fwd_threads() { return kSparse ? 512 : 192; }
+constexpr int kGatherThreads = 256;
+constexpr int kRegSoftmax = 224, kRegGather = 80, kRegMma = 64;
+constexpr int kRegPool = 128 * kRegSoftmax + 256 * kRegGather + 128 * kRegMma;
+template <bool kSparse>
+__host__ __device__ constexpr int mma_warp() { return kSparse ? 12 : 4; }
 
 template <int D>
 struct FwdCfg {
@@ -41,13 +57,15 @@ struct FwdCfg {
   static constexpr int kBar = kV + kStages * kTile;
   static constexpr int kNumBars = 1 + 4 * kStages + 4 + 4;
   static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kIdxSlots = 3;              // sparse: index chunks of 128 keys in flight
+  static constexpr int kIdx = kMisc + 16;
+  static constexpr int kBytes = kIdx + kIdxSlots * 128 * 4;
   static constexpr int kAlloc = kBytes + 1024;
   static constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
 };
 
 template <int D, bool kSparse, int kEpi, bool kPV>
-__global__ void __launch_bounds__(kFwdThreads, 1)
+__global__ void __launch_bounds__(fwd_threads<kSparse>(), 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const TcAttnParams p) {
   using L = FwdCfg<D>;
@@ -76,11 +94,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint32_t* st = p.status;
 
   if (tid == 0) {
-    mbar_init(q_full, 1);
+    const uint32_t fill = kSparse ? kGatherThreads : 1;  // sparse: every gather thread arrives; dense: one TMA arm
+    mbar_init(q_full, fill);
     for (int s = 0; s < S; ++s) {
-      mbar_init(k_full + s, 1);
+      mbar_init(k_full + s, fill);
       mbar_init(k_empty + s, 1);
-      mbar_init(v_full + s, 1);
+      mbar_init(v_full + s, fill);
       mbar_init(v_empty + s, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -93,7 +112,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     mbar_init(drain, 1);
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == mma_warp<kSparse>()) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -103,168 +122,175 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t tS = tmem + L::kColS, tO = tmem + L::kColO, tP = tmem + L::kColP;
 
-  if (warp == 5) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_map(&map_q);
-      tma_prefetch_map(&map_k);
-      if (kPV) tma_prefetch_map(&map_v);
-    }
-    const int oob_row = p.BH * p.N;  // any row >= BH*N reads as zeros
-    const int32_t* idxg = kSparse ? p.idx + (size_t(bh) * p.G + tile) * size_t(p.K) : nullptr;
-    // rows 4*lane .. 4*lane+3 of key tile j (sparse): global row ids of the gathered keys
-    auto key_rows = [&](int j, int (&r)[4]) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int slot = j * 128 + 4 * lane + i;
-        int row = oob_row;
-        if (slot < nkv) {
-          const int t = __ldg(idxg + slot);
-          if (t < 0 || t >= p.N) raise_status(st, kStatusBounds);
-          else row = bh * p.N + t;
-        }
-        r[i] = row;
-      }
-    };
-    // Q tile
-    if constexpr (kSparse) {
-      int r[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int row = 4 * lane + i;
-        int g = oob_row;
-        if (row < p.C) {
-          const int t = __ldg(p.perm + size_t(bh) * p.N_pad + size_t(tile) * p.C + row);
-          if (t < 0 || t >= p.N_pad) raise_status(st, kStatusBounds);
-          else if (t < p.N) g = bh * p.N + t;
-        }
-        r[i] = g;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(q_full, L::kTile);
-      __syncwarp();
-#pragma unroll
-      for (int rg = 0; rg < D / 64; ++rg)
-        tma_gather4(sbase + L::kQ + rg * kRegion + lane * 512, &map_q, rg * 64, r[0], r[1], r[2], r[3],
-                    smem_u32(q_full));
-    } else {
+  // Registers move between warpgroups with setmaxnreg (sparse only): each
+  // warpgroup executes its own instruction at the top of its role branch, so the
+  // role code is dominated by its register budget.
+  const bool producer = kSparse ? (warp >= 4 && warp < 12) : (warp == 5);
+  if (producer) {
+    if constexpr (kSparse) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegGather));
+    if constexpr (!kSparse) {
+      // ---------------------------------------------------------- dense: one TMA producer warp
       if (lane == 0) {
+        tma_prefetch_map(&map_q);
+        tma_prefetch_map(&map_k);
+        if (kPV) tma_prefetch_map(&map_v);
         mbar_arrive_expect_tx(q_full, L::kTile);
 #pragma unroll
         for (int rg = 0; rg < D / 64; ++rg)
           tma_load_3d(sbase + L::kQ + rg * kRegion, &map_q, rg * 64, tile * 128, bh, smem_u32(q_full));
       }
-    }
-    // K_i then V_{i-1}: K runs one tile ahead of V, as the MMA order needs.
-    int kr[4] = {0, 0, 0, 0}, vr[4] = {0, 0, 0, 0}, nr[4] = {0, 0, 0, 0};
-    if (kSparse) key_rows(0, nr);
-    int k_armed = 0, v_armed = 0;
-    bool ok = true;
-    for (int i = 0; i <= T && ok; ++i) {
-      if (i < T) {
-        const int s = i % S;
-        const uint32_t u = uint32_t(i / S);
+      // K_i then V_{i-1}: K runs one tile ahead of V, as the MMA order needs.
+      int k_armed = 0, v_armed = 0;
+      bool ok = true;
+      for (int i = 0; i <= T && ok; ++i) {
+        if (i < T) {
+          const int s = i % S;
+          const uint32_t u = uint32_t(i / S);
+          bool w = true;
+          if (lane == 0) w = mbar_wait(k_empty + s, (u & 1) ^ 1, st);
+          ok = __shfl_sync(0xffffffffu, w, 0);
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(k_full + s, L::kTile);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) kr[q] = nr[q];
-        if (kSparse && i + 1 < T) key_rows(i + 1, nr);  // prefetch next tile's indices
-        bool w = true;
-        if (lane == 0) w = mbar_wait(k_empty + s, (u & 1) ^ 1, st);
-        ok = __shfl_sync(0xffffffffu, w, 0);
-        if (!ok) break;
-        if (lane == 0) mbar_arrive_expect_tx(k_full + s, L::kTile);
-        __syncwarp();
-        const uint32_t dst = sbase + L::kK + s * L::kTile;
-        if constexpr (kSparse) {
-#pragma unroll
-          for (int rg = 0; rg < D / 64; ++rg)
-            tma_gather4(dst + rg * kRegion + lane * 512, &map_k, rg * 64, kr[0], kr[1], kr[2], kr[3],
-                        smem_u32(k_full + s));
-        } else if (lane == 0) {
-#pragma unroll
-          for (int rg = 0; rg < D / 64; ++rg)
-            tma_load_3d(dst + rg * kRegion, &map_k, rg * 64, i * 128, bh, smem_u32(k_full + s));
+            for (int rg = 0; rg < D / 64; ++rg)
+              tma_load_3d(sbase + L::kK + s * L::kTile + rg * kRegion, &map_k, rg * 64, i * 128, bh,
+                          smem_u32(k_full + s));
+          }
+          k_armed = i + 1;
         }
-        k_armed = i + 1;
-      }
-      if (kPV && i >= 1) {
-        const int j = i - 1, s = j % S;
-        const uint32_t u = uint32_t(j / S);
-        bool w = true;
-        if (lane == 0) w = mbar_wait(v_empty + s, (u & 1) ^ 1, st);
-        ok = __shfl_sync(0xffffffffu, w, 0);
-        if (!ok) break;
-        if (lane == 0) mbar_arrive_expect_tx(v_full + s, L::kTile);
-        __syncwarp();
-        const uint32_t dst = sbase + L::kV + s * L::kTile;
-        if constexpr (kSparse) {
+        if (kPV && i >= 1) {
+          const int j = i - 1, s = j % S;
+          const uint32_t u = uint32_t(j / S);
+          bool w = true;
+          if (lane == 0) w = mbar_wait(v_empty + s, (u & 1) ^ 1, st);
+          ok = __shfl_sync(0xffffffffu, w, 0);
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(v_full + s, L::kTile);
 #pragma unroll
-          for (int rg = 0; rg < D / 64; ++rg)
-            tma_gather4(dst + rg * kRegion + lane * 512, &map_v, rg * 64, vr[0], vr[1], vr[2], vr[3],
-                        smem_u32(v_full + s));
-        } else if (lane == 0) {
-#pragma unroll
-          for (int rg = 0; rg < D / 64; ++rg)
-            tma_load_3d(dst + rg * kRegion, &map_v, rg * 64, j * 128, bh, smem_u32(v_full + s));
-        }
-        v_armed = j + 1;
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) vr[q] = kr[q];
-    }
-    if (!ok && lane == 0) raise_status(st, kStatusTimeout);
-    // Let every armed copy land before the CTA can exit (normally already done).
-    if (lane == 0) {
-      mbar_wait(q_full, 0, st);
-      for (int t = (k_armed > S ? k_armed - S : 0); t < k_armed; ++t) mbar_wait(k_full + t % S, (t / S) & 1, st);
-      for (int t = (v_armed > S ? v_armed - S : 0); t < v_armed; ++t) mbar_wait(v_full + t % S, (t / S) & 1, st);
-    }
-    __syncwarp();
-  } else if (warp == 4) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
-      bool ok = mbar_wait(q_full, 0, st);
-      bool issued = false;
-      auto issue_pv = [&](int i) -> bool {
-        const int s = i % S;
-        const uint32_t u = uint32_t(i / S);
-        if (!mbar_wait(v_full + s, u & 1, st)) return false;
-        if (!mbar_wait(p_full, uint32_t(i) & 1, st)) return false;
-        tc_fence_after();
-        const uint32_t vb = sbase + L::kV + s * L::kTile;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          tc_mma_ts(tO, tP + ks * 8, desc_mnmajor(vb, ks), kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
-        tc_commit(p_empty);
-        tc_commit(v_empty + s);
-        return true;
-      };
-      for (int j = 0; ok && j < T; ++j) {
-        const int s = j % S, b = j & 1;
-        const uint32_t u = uint32_t(j / S), ub = uint32_t(j >> 1);
-        ok = mbar_wait(k_full + s, u & 1, st) && mbar_wait(s_free + b, (ub & 1) ^ 1, st);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t kb = sbase + L::kK + s * L::kTile;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          tc_mma_ss(tS + b * 128, desc_kmajor(sbase + L::kQ, ks), desc_kmajor(kb, ks), kIdescQK, ks > 0 ? 1u : 0u);
-        tc_commit(s_full + b);
-        tc_commit(k_empty + s);
-        issued = true;
-        if (kPV && j >= 1) ok = issue_pv(j - 1);
-      }
-      if (ok && kPV && T > 0) ok = issue_pv(T - 1);
-      if (ok) tc_commit(o_done);
-      if (!ok) {
-        raise_status(st, kStatusTimeout);
-        if (issued) {
-          tc_commit(drain);
-          mbar_wait(drain, 0, st);
+            for (int rg = 0; rg < D / 64; ++rg)
+              tma_load_3d(sbase + L::kV + s * L::kTile + rg * kRegion, &map_v, rg * 64, j * 128, bh,
+                          smem_u32(v_full + s));
+          }
+          v_armed = j + 1;
         }
       }
+      if (!ok && lane == 0) raise_status(st, kStatusTimeout);
+      // Let every armed copy land before the CTA can exit (normally already done).
+      if (lane == 0) {
+        mbar_wait(q_full, 0, st);
+        for (int t = (k_armed > S ? k_armed - S : 0); t < k_armed; ++t) mbar_wait(k_full + t % S, (t / S) & 1, st);
+        for (int t = (v_armed > S ? v_armed - S : 0); t < v_armed; ++t) mbar_wait(v_full + t % S, (t / S) & 1, st);
+      }
+      __syncwarp();
+    } else {
+      // ---------------------------------------------------------- sparse: eight cp.async gather warps
+      // Each thread copies 16-byte chunks of gathered rows into the swizzled
+      // stage (a warp instruction covers whole 128-byte row segments). Per tile
+      // j one cp.async group holds K_j, V_j and the index chunk of tile j+kLag;
+      // group j is retired (waited, proxy-fenced, arrived on the full barriers)
+      // kLag iterations later, so the row loads of kLag tiles are in flight.
+      constexpr int kLag = L::kIdxSlots - 1;
+      constexpr int kChunks = D / 8;               // 16-byte chunks per row
+      constexpr int kRowsPerIt = kGatherThreads / kChunks;  // rows covered by one pass of the gather threads
+      constexpr int kPasses = 128 / kRowsPerIt;
+      const int pt = tid - 128;  // 0..255
+      const int ch = pt % kChunks, r0 = pt / kChunks;
+      int32_t* ring = reinterpret_cast<int32_t*>(smem + L::kIdx);  // [kIdxSlots][128]
+      // decision of the leader for iteration j lives in stop[j & 1], so a slow
+      // reader of iteration j never sees the leader's write for iteration j + 1
+      volatile int* stop = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+      const int32_t* idxg = p.idx + (size_t(bh) * p.G + tile) * size_t(p.K);
+      const int32_t* permg = p.perm + size_t(bh) * p.N_pad + size_t(tile) * p.C;
+      const __nv_bfloat16* qb = p.q + size_t(bh) * p.N * D;
+      const __nv_bfloat16* kb = p.k + size_t(bh) * p.N * D;
+      const __nv_bfloat16* vb = p.v + size_t(bh) * p.N * D;
+      // group 0: the Q rows of the group (through perm) and index chunks of tiles 0..kLag-1
+#pragma unroll 4
+      for (int it = 0; it < kPasses; ++it) {
+        const int row = it * kRowsPerIt + r0;
+        int t = -1;
+        if (row < p.C) {
+          const int v = __ldg(permg + row);
+          if (v < 0 || v >= p.N_pad) raise_status(st, kStatusBounds);
+          else if (v < p.N) t = v;
+        }
+        cp_async16(sbase + L::kQ + sw128_off(row, ch), qb + size_t(t < 0 ? 0 : t) * D + ch * 8, t >= 0);
+      }
+#pragma unroll
+      for (int tt = 0; tt < kLag; ++tt)
+        for (int e = pt; e < 128; e += kGatherThreads) {
+          const int slot = tt * 128 + e;
+          cp_async4(smem_u32(ring + tt * 128 + e), idxg + (slot < nkv ? slot : 0), slot < nkv);
+        }
+      cp_async_commit();
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      mbar_arrive(q_full);
+      bool ok = true;
+      int issued = 0;
+      for (int j = 0; j < T; ++j) {
+        const int s = j % S;
+        if (j >= kLag) {  // retire tile j - kLag (also completes the index chunk of tile j)
+          cp_async_wait<kLag - 1>();
+          fence_proxy_async_smem();
+          mbar_arrive(k_full + (j - kLag) % S);
+          mbar_arrive(v_full + (j - kLag) % S);
+        }
+        if (pt == 0) {
+          int stp = 0;
+          if (!mbar_wait(v_empty + s, ((j / S) & 1) ^ 1, st)) {  // PV of tile j - S done: stage free
+            raise_status(st, kStatusTimeout);
+            stp = 1;
+          }
+          stop[j & 1] = stp;
+        }
+        named_bar_sync(1, kGatherThreads);
+        if (stop[j & 1]) {
+          ok = false;
+          break;
+        }
+        const int32_t* rt = ring + (j % L::kIdxSlots) * 128;
+        const uint32_t dk = sbase + L::kK + s * L::kTile, dv = sbase + L::kV + s * L::kTile;
+        // all of this thread's row indices first, then the copies back to back: a
+        // load between two copies would serialise the warp on its latency
+        int toks[kPasses];
+#pragma unroll
+        for (int it = 0; it < kPasses; ++it) {
+          const int row = it * kRowsPerIt + r0;
+          toks[it] = (j * 128 + row < nkv) ? rt[row] : -1;
+        }
+#pragma unroll
+        for (int it = 0; it < kPasses; ++it) {
+          const int row = it * kRowsPerIt + r0;
+          int t = toks[it];
+          if (t >= p.N || (t < 0 && j * 128 + row < nkv)) {
+            raise_status(st, kStatusBounds);
+            t = -1;
+          }
+          const size_t off = size_t(t < 0 ? 0 : t) * D + ch * 8;
+          cp_async16(dk + sw128_off(row, ch), kb + off, t >= 0);
+          cp_async16(dv + sw128_off(row, ch), vb + off, t >= 0);
+        }
+        for (int e = pt; e < 128; e += kGatherThreads) {
+          const int tn = j + kLag, slot = tn * 128 + e;
+          cp_async4(smem_u32(ring + (tn % L::kIdxSlots) * 128 + e), idxg + (slot < nkv ? slot : 0), slot < nkv);
+        }
+        cp_async_commit();
+        issued = j + 1;
+      }
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      if (ok) {
+        for (int t = (issued > kLag ? issued - kLag : 0); t < issued; ++t) {
+          mbar_arrive(k_full + t % S);
+          mbar_arrive(v_full + t % S);
+        }
+      }
     }
-  } else {
+  } else if (warp < 4) {
+    if constexpr (kSparse) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegSoftmax));
     // ------------------------------------------------------------ softmax (thread = query row)
     const int row = tid;
     const uint32_t lane_off = uint32_t(warp * 32) << 16;
@@ -369,10 +395,60 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
     }
     if (!ok && row == 0) raise_status(st, kStatusTimeout);
+  } else {
+    // dense: warp 4; sparse: warpgroup 3 (warp 12 issues, warps 13-15 idle)
+    if constexpr (kSparse) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegMma));
+    if (warp == mma_warp<kSparse>()) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
+      bool ok = mbar_wait(q_full, 0, st);
+      bool issued = false;
+      auto issue_pv = [&](int i) -> bool {
+        const int s = i % S;
+        const uint32_t u = uint32_t(i / S);
+        if (!mbar_wait(v_full + s, u & 1, st)) return false;
+        if (!mbar_wait(p_full, uint32_t(i) & 1, st)) return false;
+        tc_fence_after();
+        const uint32_t vb = sbase + L::kV + s * L::kTile;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          tc_mma_ts(tO, tP + ks * 8, desc_mnmajor(vb, ks), kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
+        tc_commit(p_empty);
+        tc_commit(v_empty + s);
+        return true;
+      };
+      for (int j = 0; ok && j < T; ++j) {
+        const int s = j % S, b = j & 1;
+        const uint32_t u = uint32_t(j / S), ub = uint32_t(j >> 1);
+        ok = mbar_wait(k_full + s, u & 1, st) && mbar_wait(s_free + b, (ub & 1) ^ 1, st);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t kb = sbase + L::kK + s * L::kTile;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          tc_mma_ss(tS + b * 128, desc_kmajor(sbase + L::kQ, ks), desc_kmajor(kb, ks), kIdescQK, ks > 0 ? 1u : 0u);
+        tc_commit(s_full + b);
+        tc_commit(k_empty + s);
+        issued = true;
+        if (kPV && j >= 1) ok = issue_pv(j - 1);
+      }
+      if (ok && kPV && T > 0) ok = issue_pv(T - 1);
+      if (ok) tc_commit(o_done);
+      if (!ok) {
+        raise_status(st, kStatusTimeout);
+        if (issued) {
+          tc_commit(drain);
+          mbar_wait(drain, 0, st);
+        }
+      }
+    }
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == mma_warp<kSparse>()) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -384,9 +460,10 @@ cudaError_t launch_fwd(const TcAttnParams& p, cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
   const uint64_t rows = uint64_t(p.BH) * p.N;
   bool ok;
-  if (kSparse) {
-    ok = make_gather_map(&mq, p.q, rows, D) && make_gather_map(&mk, p.k, rows, D) &&
-         make_gather_map(&mv, p.v, rows, D);
+  if (kSparse) {  // rows are gathered with cp.async; the maps are unused placeholders
+    ok = make_gather_map(&mq, p.q, rows, D);
+    mk = mq;
+    mv = mq;
   } else {
     ok = make_tile_map(&mq, p.q, p.BH, p.N, D, 128) && make_tile_map(&mk, p.k, p.BH, p.N, D, 128) &&
          make_tile_map(&mv, p.v, p.BH, p.N, D, 128);
@@ -395,8 +472,15 @@ cudaError_t launch_fwd(const TcAttnParams& p, cudaStream_t stream) {
   auto kern = attn_fwd_kernel<D, kSparse, kEpi, kPV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
+  if (kSparse) {
+    // setmaxnreg.inc waits for registers released by the other warpgroups: never
+    // launch unless the rebalanced split fits in what the block is launched with
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+    if (fa.numRegs * fwd_threads<kSparse>() < kRegPool || fa.numRegs < kRegGather) return cudaErrorInvalidValue;
+  }
   dim3 grid(p.tiles_per_head, p.BH);
-  kern<<<grid, kFwdThreads, L::kAlloc, stream>>>(mq, mk, mv, p);
+  kern<<<grid, fwd_threads<kSparse>(), L::kAlloc, stream>>>(mq, mk, mv, p);
   note_launches(1);
   return cudaGetLastError();
 }

@@ -111,7 +111,9 @@ __global__ void __launch_bounds__(kThreads, 1) colsum_tc_kernel(const TcColsumPa
       mbar_arrive(q_full);
     }
     const __nv_bfloat16* kb = p.k + size_t(bh) * p.N * D;
-    volatile int* grp_stop = abort_flag + 1;  // written by the producer leader only
+    // the leader's decision for iteration j lives in grp_stop[j & 1] (written by
+    // the leader only), so a slow reader never sees the next iteration's write
+    volatile int* grp_stop = abort_flag + 1;
     int j = 0;
     for (; j < T; ++j) {
       const int s = j & 1;
@@ -123,10 +125,10 @@ __global__ void __launch_bounds__(kThreads, 1) colsum_tc_kernel(const TcColsumPa
           *abort_flag = 1;
           stop = 1;
         }
-        *grp_stop = stop;
+        grp_stop[j & 1] = stop;
       }
       named_bar_sync(1, 128);
-      if (*grp_stop) break;
+      if (grp_stop[j & 1]) break;
 #pragma unroll 4
       for (int it = 0; it < D / 8; ++it) {
         const int id = it * 128 + pt, row = id / (D / 8), ch = id % (D / 8);

@@ -66,6 +66,11 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
   const uint32_t n = valid ? 16u : 0u;  // src-size 0 writes 16 zero bytes
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
 }
+// 4-byte variant (through L1), for index lists without 16-byte alignment.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
+  const uint32_t n = valid ? 4u : 0u;
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
