@@ -108,6 +108,24 @@ mcs_status mcs_anchor_select(const mcs_desc *desc, const void *q, const void *k,
                              const float *lse, int K, int32_t *idx, float *mass,
                              void *ws, size_t ws_bytes, mcs_stream stream);
 
+/* Anchor selection for callers that cannot allocate device memory (the method
+ * has no counterpart: this is a deployment variant of mcs_anchor_select).
+ * Code that runs where cudaMalloc is unavailable or forbidden (inside a
+ * capture that must not allocate, a host framework that owns the device heap
+ * and gives plug-ins no allocator, a loop that cannot afford cudaMalloc's
+ * synchronisation) can call this instead: the pass-2 score rows live in one
+ * fixed 64 MiB array inside the library (held by every GPU that loads it until
+ * the process exits), so the call allocates nothing. Same arguments and results
+ * as mcs_anchor_select, except that lse is required (pass 1 is not computed
+ * here) and there is no workspace. Limits: N * 4 bytes (one score row) must fit
+ * in the 64 MiB array, i.e. N <= 16,777,216, else MCS_ERR_UNSUPPORTED. The
+ * first call on a device looks up the array's device address with that device
+ * current; make that first call before any stream capture. All calls share the
+ * array and leave their scores in it (nothing needs clearing: each call writes
+ * every score it reads); calls whose kernels overlap on the GPU race on it. */
+mcs_status mcs_anchor_select_noalloc(const mcs_desc *desc, const void *q, const void *k, const int32_t *perm,
+                                     const float *lse, int K, int32_t *idx, float *mass, mcs_stream stream);
+
 /* [grouping] + [residual] token-gather sparse attention. For every group g and
  * real member i: o_i = sum_{j in idx[g]} softmax_{idx[g]}(scale q_i.k_j) v_j
  * (renormalised over the kept keys), plus residual_i when residual != NULL.

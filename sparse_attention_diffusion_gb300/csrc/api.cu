@@ -170,6 +170,10 @@ mcs_status sparse_impl(const Dims& dm, int epi, const void* q, const void* k, co
 
 namespace mcs {
 void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
+uint32_t* status_word_for_current_device() {
+  uint32_t* st = nullptr;
+  return device_state(&st, nullptr) == MCS_OK ? st : nullptr;
+}
 }  // namespace mcs
 
 extern "C" {

@@ -25,7 +25,8 @@ enum Epilogue : int {
   kEpiStoreResidual = 2 // r = o_dense - attention    (anchor step)
 };
 
-// Host-side launch bookkeeping (defined in api.cu).
+// Host-side launch bookkeeping and the device status word (defined in api.cu).
 void note_launches(int n);
+uint32_t* status_word_for_current_device();  // null if the CUDA runtime call failed
 
 }  // namespace mcs

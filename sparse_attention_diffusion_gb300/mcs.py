@@ -23,7 +23,7 @@ MCS_F32, MCS_BF16 = 0, 1
 EXPORTS = ("mcs_workspace_size", "mcs_group_pddp", "mcs_dense_attn", "mcs_anchor_select",
            "mcs_sparse_attn_gather", "mcs_anchor_residual", "mcs_residual_store", "mcs_residual_apply",
            "mcs_check_status", "mcs_status_string", "mcs_launch_count", "mcs_selftest_tc_mma",
-           "mcs_selftest_tma_gather")
+           "mcs_selftest_tma_gather", "mcs_anchor_select_noalloc")
 
 
 class McsError(RuntimeError):
@@ -71,6 +71,7 @@ def load(build_if_missing: bool = False):
         "mcs_launch_count": (ctypes.c_uint64, []),
         "mcs_selftest_tc_mma": (I, [P, P, P, I, ctypes.c_uint32, ctypes.c_uint32, S]),
         "mcs_selftest_tma_gather": (I, [P, I, P, P, S]),
+        "mcs_anchor_select_noalloc": (I, [D, P, P, P, P, I, P, P, S]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -146,6 +147,13 @@ def mcs_anchor_select(desc, q, k, perm, lse, K, idx, mass, ws, stream=None):
     _check("mcs_anchor_select", load().mcs_anchor_select(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(perm), _ptr(lse),
                                                          int(K), _ptr(idx), _ptr(mass), _ptr(ws), ws.numel(),
                                                          _stream(stream)))
+
+
+def mcs_anchor_select_noalloc(desc, q, k, perm, lse, K, idx, mass, stream=None):
+    """mcs_anchor_select without a workspace (scores kept in the library's fixed device array)."""
+    _check("mcs_anchor_select_noalloc", load().mcs_anchor_select_noalloc(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(perm),
+                                                                         _ptr(lse), int(K), _ptr(idx), _ptr(mass),
+                                                                         _stream(stream)))
 
 
 def mcs_sparse_attn_gather(desc, q, k, v, perm, idx, K, residual, o, stream=None):
