@@ -1,0 +1,134 @@
+// Softmax and epilogue of the tcgen05 attention kernels (dense and sparse), run
+// by warps 0-3: one thread per query row, which is the TMEM lane the row's
+// accumulators live on.
+#pragma once
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "tc_common.cuh"
+
+namespace mcs {
+
+struct SoftmaxSync {
+  uint64_t* s_full;   // [2] S buffer b written by the MMA
+  uint64_t* s_free;   // [2] S buffer b read (128 arrivals)
+  uint64_t* p_full;   // P written to TMEM (128 arrivals)
+  uint64_t* p_empty;  // PV of the previous tile done (O stable, P free)
+};
+
+// Online base-2 softmax over T tiles of 128 keys (nkv keys in all). For tile j:
+// load the S row from TMEM buffer j%2, update the running max m (log2 units,
+// rescaled lazily: only when the max grows by more than 2^8) and the running sum
+// l, write P = 2^(s*scale_log2 - m) to TMEM as bf16 pairs and, when the max
+// moved, rescale the O accumulator row in TMEM. The exponentials are computed
+// before waiting for the previous PV so they overlap it.
+// Returns false if a bounded wait ran out.
+template <int D, bool kPV>
+__device__ __forceinline__ bool softmax_rows(int T, int nkv, uint32_t tS, uint32_t tO, uint32_t tP, uint32_t lane_off,
+                                             float sl2, const SoftmaxSync& sy, const uint32_t* st, float& m_out,
+                                             float& l_out) {
+  float m = -INFINITY, l = 0.f;
+  bool ok = true;
+  for (int j = 0; j < T; ++j) {
+    const int b = j & 1;
+    const uint32_t ub = uint32_t(j >> 1);
+    ok = warp_all(mbar_wait(sy.s_full + b, ub & 1, st));
+    if (!ok) break;
+    tc_fence_after();
+    uint32_t r[128];
+    tmem_ld128(tS + lane_off + b * 128, r);
+    tc_fence_before();
+    mbar_arrive(sy.s_free + b);
+    const int nvalid = min(128, nkv - j * 128);
+    if (nvalid < 128) {  // last, partial tile: logits of missing keys become -inf (p = 0)
+#pragma unroll
+      for (int c = 0; c < 128; ++c)
+        if (c >= nvalid) r[c] = __float_as_uint(-INFINITY);
+    }
+    // independent partial maxima and sums: one warp per scheduler runs this, so
+    // a single dependent chain of 128 max / 64 add operations would be pure latency
+    float mp[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mp[i] = __uint_as_float(r[i]);
+#pragma unroll
+    for (int c = 8; c < 128; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(r[c]));
+    const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+    const float m_new = fmaxf(m, mx * sl2);
+    const bool need = m_new > m + 8.f;
+    const float m_use = need ? m_new : m;
+    const float alpha = need ? ex2_approx(m - m_new) : 1.f;
+    const float neg_m = -m_use;
+    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t pk[64];
+#pragma unroll
+    for (int c = 0; c < 64; ++c) {
+      const float p0 = ex2_approx(fmaf(__uint_as_float(r[2 * c]), sl2, neg_m));
+      const float p1 = ex2_approx(fmaf(__uint_as_float(r[2 * c + 1]), sl2, neg_m));
+      ls[c & 3] += p0 + p1;
+      pk[c] = pack_bf16x2(p0, p1);
+    }
+    const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+    l = l * alpha + lsum;
+    m = m_use;
+    if constexpr (kPV) {
+      ok = warp_all(mbar_wait(sy.p_empty, (uint32_t(j) & 1) ^ 1, st));  // PV of tile j-1 done
+      if (!ok) break;
+      tc_fence_after();
+      if (__any_sync(0xffffffffu, need && j > 0)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + lane_off + c * 32, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + lane_off + c * 32, o);
+        }
+      }
+      tmem_st64(tP + lane_off, pk);
+      tc_fence_before();
+      mbar_arrive(sy.p_full);
+    }
+  }
+  m_out = m;
+  l_out = l;
+  return ok;
+}
+
+// Epilogue for one row: O / l from TMEM, optionally plus (add-residual) or
+// subtracted from (store-residual) a bf16 row, rounded once to bf16 and stored.
+// Every thread of the warp must call it (the TMEM loads are warp-collective);
+// rows with tok < 0 load but store nothing.
+template <int D, int kEpi>
+__device__ __forceinline__ void store_row(uint32_t tO, uint32_t lane_off, int tok, size_t rowoff, float inv_l,
+                                          __nv_bfloat16* dst, const __nv_bfloat16* res_in) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32(tO + lane_off + c * 32, o);
+    if (tok >= 0 && dst != nullptr) {
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float o8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o8[i] = __uint_as_float(o[q4 * 8 + i]) * inv_l;
+        const size_t off = rowoff + c * 32 + q4 * 8;
+        if constexpr (kEpi != kEpiPlain) {
+          const uint4 rv = *reinterpret_cast<const uint4*>(res_in + off);
+          const __nv_bfloat16* rb = reinterpret_cast<const __nv_bfloat16*>(&rv);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            o8[i] = (kEpi == kEpiAddResidual) ? o8[i] + __bfloat162float(rb[i]) : __bfloat162float(rb[i]) - o8[i];
+        }
+        uint4 w;
+        w.x = pack_bf16x2(o8[0], o8[1]);
+        w.y = pack_bf16x2(o8[2], o8[3]);
+        w.z = pack_bf16x2(o8[4], o8[5]);
+        w.w = pack_bf16x2(o8[6], o8[7]);
+        *reinterpret_cast<uint4*>(dst + off) = w;
+      }
+    }
+  }
+}
+
+}  // namespace mcs
