@@ -7,26 +7,31 @@
 // [MC-Sparse summary: residual paragraph].
 //
 // One CTA per group, 512 threads in four warpgroups:
-//   warpgroup 0 (warps 0-3)   softmax, one thread per query row, and the epilogue;
-//   warpgroups 1-2 (4-11)     eight gather warps: the group's query rows (through
-//                             perm) once, then per tile of 128 keys the key and
-//                             value rows at the group's index list, as 16-byte
-//                             cp.async copies into a 3-stage, 128-byte-swizzled
-//                             ring; the index list streams through a
-//                             shared-memory ring two tiles ahead;
+//   warpgroup 0 (warps 0-3)   loads each query row into tensor memory (operand A
+//                             of S = Q K^T), then runs the softmax, one thread per
+//                             query row, and the epilogue;
+//   warpgroups 1-2 (4-11)     eight gather warps: per iteration i the key rows of
+//                             tile i and the value rows of tile i-1 (128 keys per
+//                             tile) at the group's index list, as 16-byte cp.async
+//                             copies into a 4-stage K ring and a 3-stage V ring
+//                             (128-byte swizzled); the index list streams through
+//                             a shared-memory ring two tiles ahead;
 //   warpgroup 3 (warp 12)     tensor-memory allocation and the single
 //                             MMA-issuing thread (warps 13-15 idle).
-// Per tile each gather thread reads its row indices into registers first and
-// then issues its copies back to back (a load between two copies would
-// serialise the warp on its latency); tile j's copies form one cp.async group,
-// retired (waited, proxy-fenced, arrived on the full barriers) two tiles later.
+// A K stage is released when S of its tile is done, a V stage when PV is done,
+// so key rows are fetched well ahead of their use; iteration i's copies form one
+// cp.async group, retired (waited, proxy-fenced, arrived on the full barriers)
+// two iterations later. Each gather thread reads its row indices into registers
+// before issuing its copies back to back (a load between two copies would
+// serialise the warp on its latency) and keeps them for the value rows of the
+// same tile one iteration later. The MMA thread issues P_j V_j as soon as P_j is
+// written and only puts S_{j+1} first when its key rows have already landed.
 // Row gathers of 128-byte segments are kept on the load/store path: on this GPU
 // they move far more bytes per cycle than 4-row TMA gathers, and their
 // throughput grows with the number of issuing warps. Registers are rebalanced
-// with setmaxnreg (softmax 224, gather 80, MMA 64); the launcher checks that
-// the split fits the registers the block is launched with.
-// S = Q K^T reads both operands from shared memory; PV reads P from tensor memory.
-// Tensor memory: S0 [0,128), S1 [128,256), O [256,256+D), P [384,448).
+// with setmaxnreg (softmax 224, gather 80, MMA 64); the launcher checks that the
+// split fits the registers the block is launched with.
+// Tensor memory: S0 [0,128), S1 [128,256), O [256,256+D), P [384,448), Q [448,448+D/2).
 // All waits are bounded; on a timeout the CTA flags it, lets its copies and
 // MMAs land, frees tensor memory and returns.
 #include "attn_common.cuh"
@@ -45,27 +50,26 @@ constexpr int kRegPool = 128 * kRegSoftmax + kGather * kRegGather + 128 * kRegMm
 
 template <int D>
 struct SparseCfg {
-  static constexpr int kSK = 3, kSV = 3;      // K and V stages (a tile's K and V share a stage index)
-  static constexpr int kLag = 2;              // tiles between a tile's issue and its full signal
-  static constexpr int kRingK = kLag + 1;     // index chunks of 128 keys in shared memory
+  static constexpr int kSK = 4, kSV = 3;      // K and V stages
+  static constexpr int kLag = 2;              // iterations between a copy group's issue and its retirement
+  static constexpr int kRing = kLag + 1;      // index chunks of 128 keys in shared memory
   static constexpr int kTile = (D / 64) * kRegion;
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTile;
+  static constexpr int kK = 0;
   static constexpr int kV = kK + kSK * kTile;
   static constexpr int kBar = kV + kSV * kTile;
   static constexpr int kNumBars = 1 + 2 * kSK + 2 * kSV + 4 + 4;
-  static constexpr int kMisc = kBar + kNumBars * 8;  // tmem slot, K stop flags [2], V stop flags [2]
-  static constexpr int kRing = kMisc + 32;
-  static constexpr int kBytes = kRing + kRingK * 128 * 4;
+  static constexpr int kMisc = kBar + kNumBars * 8;  // tmem slot, stop flags [2]
+  static constexpr int kIdx = kMisc + 32;
+  static constexpr int kBytes = kIdx + kRing * 128 * 4;
   static constexpr int kAlloc = kBytes + 1024;
-  static constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+  static constexpr uint32_t kColS = 0, kColO = 256, kColP = 384, kColQ = 448;
 };
 
 template <int D, int kEpi>
 __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const TcAttnParams p) {
   using L = SparseCfg<D>;
   constexpr int SK = L::kSK, SV = L::kSV, kLag = L::kLag;
-  constexpr int kChunks = D / 8;              // 16-byte chunks per row
+  constexpr int kChunks = D / 8;  // 16-byte chunks per row
   constexpr int kRowsPerPass = kGather / kChunks;
   constexpr int kPasses = 128 / kRowsPerPass;
   extern __shared__ uint8_t smem_raw[];
@@ -84,10 +88,10 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
   uint64_t* o_done = p_empty + 1;
   uint64_t* drain = o_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
-  // the gather leader's decision for iteration j lives in stop[j & 1]: a slow
-  // reader of iteration j never sees the leader's write for iteration j + 1
+  // the gather leader's decision for iteration i lives in stop[i & 1]: a slow
+  // reader of iteration i never sees the leader's write for iteration i + 1
   volatile int* stop = reinterpret_cast<volatile int*>(smem + L::kMisc + 8);
-  int32_t* ring = reinterpret_cast<int32_t*>(smem + L::kRing);  // [kRingK][128]
+  int32_t* ring = reinterpret_cast<int32_t*>(smem + L::kIdx);  // [kRing][128]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.y, g = blockIdx.x;
@@ -97,7 +101,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
   const int32_t* idxg = p.idx + (size_t(bh) * p.G + g) * size_t(p.K);
 
   if (tid == 0) {
-    mbar_init(q_full, kGather);
+    mbar_init(q_full, 128);
     for (int s = 0; s < SK; ++s) {
       mbar_init(k_full + s, kGather);
       mbar_init(k_empty + s, 1);
@@ -124,11 +128,11 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem + L::kColS, tO = tmem + L::kColO, tP = tmem + L::kColP;
+  const uint32_t tS = tmem + L::kColS, tO = tmem + L::kColO, tP = tmem + L::kColP, tQ = tmem + L::kColQ;
 
   if (warp < 4) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegSoftmax));
-    // ------------------------------------------------------------ softmax, epilogue
+    // ------------------------------------------------------------ Q -> TMEM, softmax, epilogue
     const int row = tid;
     const uint32_t lane_off = uint32_t(warp * 32) << 16;
     int tok = -1;
@@ -136,6 +140,29 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
       const int v = __ldg(p.perm + size_t(bh) * p.N_pad + size_t(g) * p.C + row);
       if (v < 0 || v >= p.N_pad) raise_status(st, kStatusBounds);
       else if (v < p.N) tok = v;
+    }
+    {
+      // a bf16 row is already laid out as the packed pairs a TMEM column holds
+      uint32_t qw[64];
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + (size_t(bh) * p.N + size_t(tok < 0 ? 0 : tok)) * D);
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        const uint4 v = tok >= 0 ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+        qw[4 * c] = v.x;
+        qw[4 * c + 1] = v.y;
+        qw[4 * c + 2] = v.z;
+        qw[4 * c + 3] = v.w;
+      }
+      if constexpr (D == 128) {
+        tmem_st64(tQ + lane_off, qw);
+      } else {
+        uint32_t q32[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) q32[i] = qw[i];
+        tmem_st32(tQ + lane_off, q32);
+      }
+      tc_fence_before();
+      mbar_arrive(q_full);
     }
     float m, l;
     const SoftmaxSync sy{s_full, s_free, p_full, p_empty};
@@ -151,25 +178,11 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
   } else if (warp < 12) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegGather));
     // ------------------------------------------------------------ gather warps
-    static_assert(SK == SV, "a tile's K and V share one stage index");
     const int t = tid - 128;  // 0..255
     const int ch = t % kChunks, r0 = t / kChunks;
-    const __nv_bfloat16* qb = p.q + size_t(bh) * p.N * D;
     const __nv_bfloat16* kb = p.k + size_t(bh) * p.N * D;
     const __nv_bfloat16* vb = p.v + size_t(bh) * p.N * D;
-    const int32_t* permg = p.perm + size_t(bh) * p.N_pad + size_t(g) * p.C;
-    // group 0: the query rows (through perm) and the index chunks of tiles 0..kLag-1
-#pragma unroll 4
-    for (int it = 0; it < kPasses; ++it) {
-      const int row = it * kRowsPerPass + r0;
-      int tq = -1;
-      if (row < p.C) {
-        const int v = __ldg(permg + row);
-        if (v < 0 || v >= p.N_pad) raise_status(st, kStatusBounds);
-        else if (v < p.N) tq = v;
-      }
-      cp_async16(sbase + L::kQ + sw128_off(row, ch), qb + size_t(tq < 0 ? 0 : tq) * D + ch * 8, tq >= 0);
-    }
+    // index chunks of tiles 0..kLag-1
 #pragma unroll
     for (int tt = 0; tt < kLag; ++tt)
       for (int e = t; e < 128; e += kGather) {
@@ -178,65 +191,80 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
       }
     cp_async_commit();
     cp_async_wait<0>();
-    fence_proxy_async_smem();
-    mbar_arrive(q_full);
+    named_bar_sync(1, kGather);
+    int prev[kPasses];  // this thread's key ids of tile i-1, for its value rows
+#pragma unroll
+    for (int it = 0; it < kPasses; ++it) prev[it] = -1;
     bool ok = true;
-    int issued = 0;
-    for (int j = 0; j < T; ++j) {
-      const int s = j % SK;
-      if (j >= kLag) {  // retire tile j - kLag (also completes the index chunk of tile j)
+    int issued = 0;  // iterations whose copy group was committed
+    for (int i = 0; i <= T; ++i) {
+      if (i >= kLag) {  // retire iteration i - kLag: K of tile i-kLag, V of tile i-kLag-1
         cp_async_wait<kLag - 1>();
         fence_proxy_async_smem();
-        mbar_arrive(k_full + (j - kLag) % SK);
-        mbar_arrive(v_full + (j - kLag) % SV);
+        const int r = i - kLag;
+        if (r < T) mbar_arrive(k_full + r % SK);
+        if (r >= 1) mbar_arrive(v_full + (r - 1) % SV);
       }
       if (t == 0) {
         int stp = 0;
-        if (!mbar_wait(v_empty + s, ((j / SV) & 1) ^ 1, st)) {  // PV of tile j - S done: stage free
-          raise_status(st, kStatusTimeout);
+        if (i < T && !mbar_wait(k_empty + i % SK, ((i / SK) & 1) ^ 1, st)) stp = 1;           // S of tile i-SK done
+        if (!stp && i >= 1 && !mbar_wait(v_empty + (i - 1) % SV, (((i - 1) / SV) & 1) ^ 1, st))  // PV of tile i-1-SV
           stp = 1;
-        }
-        stop[j & 1] = stp;
+        if (stp) raise_status(st, kStatusTimeout);
+        stop[i & 1] = stp;
       }
       named_bar_sync(1, kGather);
-      if (stop[j & 1]) {
+      if (stop[i & 1]) {
         ok = false;
         break;
       }
-      const int32_t* rt = ring + (j % L::kRingK) * 128;
-      const uint32_t dk = sbase + L::kK + s * L::kTile, dv = sbase + L::kV + s * L::kTile;
       int toks[kPasses];
+      if (i < T) {
+        const int32_t* rt = ring + (i % L::kRing) * 128;
 #pragma unroll
-      for (int it = 0; it < kPasses; ++it) {
-        const int row = it * kRowsPerPass + r0;
-        toks[it] = (j * 128 + row < nkv) ? rt[row] : -1;
-      }
-#pragma unroll
-      for (int it = 0; it < kPasses; ++it) {
-        const int row = it * kRowsPerPass + r0;
-        int tk = toks[it];
-        if (tk >= p.N || (tk < 0 && j * 128 + row < nkv)) {
-          raise_status(st, kStatusBounds);
-          tk = -1;
+        for (int it = 0; it < kPasses; ++it) {
+          const int row = it * kRowsPerPass + r0;
+          int tk = (i * 128 + row < nkv) ? rt[row] : -1;
+          if (tk >= p.N || (tk < 0 && i * 128 + row < nkv)) {
+            raise_status(st, kStatusBounds);
+            tk = -1;
+          }
+          toks[it] = tk;
         }
-        const size_t off = size_t(tk < 0 ? 0 : tk) * D + ch * 8;
-        cp_async16(dk + sw128_off(row, ch), kb + off, tk >= 0);
-        cp_async16(dv + sw128_off(row, ch), vb + off, tk >= 0);
+        const uint32_t dk = sbase + L::kK + (i % SK) * L::kTile;
+#pragma unroll
+        for (int it = 0; it < kPasses; ++it) {
+          const int row = it * kRowsPerPass + r0;
+          cp_async16(dk + sw128_off(row, ch), kb + size_t(toks[it] < 0 ? 0 : toks[it]) * D + ch * 8, toks[it] >= 0);
+        }
+      }
+      if (i >= 1) {
+        const uint32_t dv = sbase + L::kV + ((i - 1) % SV) * L::kTile;
+#pragma unroll
+        for (int it = 0; it < kPasses; ++it) {
+          const int row = it * kRowsPerPass + r0;
+          cp_async16(dv + sw128_off(row, ch), vb + size_t(prev[it] < 0 ? 0 : prev[it]) * D + ch * 8, prev[it] >= 0);
+        }
       }
       for (int e = t; e < 128; e += kGather) {
-        const int tn = j + kLag, slot = tn * 128 + e;
-        cp_async4(smem_u32(ring + (tn % L::kRingK) * 128 + e), idxg + (slot < nkv ? slot : 0), slot < nkv);
+        const int tn = i + kLag, slot = tn * 128 + e;
+        cp_async4(smem_u32(ring + (tn % L::kRing) * 128 + e), idxg + (slot < nkv ? slot : 0), slot < nkv);
       }
       cp_async_commit();
-      issued = j + 1;
+      issued = i + 1;
+      if (i < T) {
+#pragma unroll
+        for (int it = 0; it < kPasses; ++it) prev[it] = toks[it];
+      }
     }
     cp_async_wait<0>();
     fence_proxy_async_smem();
-    if (ok)
-      for (int tt = (issued > kLag ? issued - kLag : 0); tt < issued; ++tt) {
-        mbar_arrive(k_full + tt % SK);
-        mbar_arrive(v_full + tt % SV);
+    if (ok) {  // iterations issued - kLag .. issued - 1 were not retired in the loop
+      for (int r = (issued > kLag ? issued - kLag : 0); r < issued; ++r) {
+        if (r < T) mbar_arrive(k_full + r % SK);
+        if (r >= 1) mbar_arrive(v_full + (r - 1) % SV);
       }
+    }
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegMma));
     // ------------------------------------------------------------ MMA issuer (warp 12)
@@ -245,6 +273,23 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
       constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
       bool ok = mbar_wait(q_full, 0, st);
       bool issued = false;
+      if (ok) tc_fence_after();
+      auto s_ready = [&](int j) {
+        return mbar_test(k_full + j % SK, uint32_t(j / SK) & 1) && mbar_test(s_free + (j & 1), (uint32_t(j >> 1) & 1) ^ 1);
+      };
+      auto issue_s = [&](int j) -> bool {
+        if (!mbar_wait(k_full + j % SK, uint32_t(j / SK) & 1, st)) return false;
+        if (!mbar_wait(s_free + (j & 1), (uint32_t(j >> 1) & 1) ^ 1, st)) return false;
+        tc_fence_after();
+        const uint32_t kt = sbase + L::kK + (j % SK) * L::kTile;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          tc_mma_ts(tS + (j & 1) * 128, tQ + ks * 8, desc_kmajor(kt, ks), kIdescQK, ks > 0 ? 1u : 0u);
+        tc_commit(s_full + (j & 1));
+        tc_commit(k_empty + j % SK);
+        issued = true;
+        return true;
+      };
       auto issue_pv = [&](int i) -> bool {
         const int s = i % SV;
         if (!mbar_wait(v_full + s, uint32_t(i / SV) & 1, st)) return false;
@@ -258,21 +303,18 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
         tc_commit(v_empty + s);
         return true;
       };
+      if (ok && T > 0) ok = issue_s(0);
       for (int j = 0; ok && j < T; ++j) {
-        const int s = j % SK, b = j & 1;
-        ok = mbar_wait(k_full + s, uint32_t(j / SK) & 1, st) && mbar_wait(s_free + b, (uint32_t(j >> 1) & 1) ^ 1, st);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t kt = sbase + L::kK + s * L::kTile;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          tc_mma_ss(tS + b * 128, desc_kmajor(sbase + L::kQ, ks), desc_kmajor(kt, ks), kIdescQK, ks > 0 ? 1u : 0u);
-        tc_commit(s_full + b);
-        tc_commit(k_empty + s);
-        issued = true;
-        if (j >= 1) ok = issue_pv(j - 1);
+        // S_{j+1} and PV_j are independent: take S_{j+1} first only if it can go now
+        const bool s_next = j + 1 < T;
+        bool s_done = false;
+        if (s_next && s_ready(j + 1)) {
+          ok = issue_s(j + 1);
+          s_done = true;
+        }
+        if (ok) ok = issue_pv(j);
+        if (ok && s_next && !s_done) ok = issue_s(j + 1);
       }
-      if (ok && T > 0) ok = issue_pv(T - 1);
       if (ok) tc_commit(o_done);
       if (!ok) {
         raise_status(st, kStatusTimeout);
