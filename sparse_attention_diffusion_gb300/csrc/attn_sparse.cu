@@ -7,13 +7,12 @@
 // [MC-Sparse summary: residual paragraph].
 //
 // One CTA per group, 512 threads in four warpgroups:
-//   warpgroup 0 (warps 0-3)   loads each query row into tensor memory (operand A
-//                             of S = Q K^T), then runs the softmax, one thread per
-//                             query row, and the epilogue;
-//   warpgroups 1-2 (4-11)     eight gather warps: per iteration i the key rows of
+//   warpgroup 0 (warps 0-3)   softmax, one thread per query row, and the epilogue;
+//   warpgroups 1-2 (4-11)     eight gather warps: the group's query rows (through
+//                             perm) once, then per iteration i the key rows of
 //                             tile i and the value rows of tile i-1 (128 keys per
 //                             tile) at the group's index list, as 16-byte cp.async
-//                             copies into a 4-stage K ring and a 3-stage V ring
+//                             copies into a 3-stage K ring and a 3-stage V ring
 //                             (128-byte swizzled); the index list streams through
 //                             a shared-memory ring two tiles ahead;
 //   warpgroup 3 (warp 12)     tensor-memory allocation and the single
@@ -31,7 +30,8 @@
 // throughput grows with the number of issuing warps. Registers are rebalanced
 // with setmaxnreg (softmax 224, gather 80, MMA 64); the launcher checks that the
 // split fits the registers the block is launched with.
-// Tensor memory: S0 [0,128), S1 [128,256), O [256,256+D), P [384,448), Q [448,448+D/2).
+// S = Q K^T reads both operands from shared memory; PV reads P from tensor memory.
+// Tensor memory: S0 [0,128), S1 [128,256), O [256,256+D), P [384,448).
 // All waits are bounded; on a timeout the CTA flags it, lets its copies and
 // MMAs land, frees tensor memory and returns.
 #include "attn_common.cuh"
@@ -50,11 +50,12 @@ constexpr int kRegPool = 128 * kRegSoftmax + kGather * kRegGather + 128 * kRegMm
 
 template <int D>
 struct SparseCfg {
-  static constexpr int kSK = 4, kSV = 3;      // K and V stages
+  static constexpr int kSK = 3, kSV = 3;      // K and V stages
   static constexpr int kLag = 2;              // iterations between a copy group's issue and its retirement
   static constexpr int kRing = kLag + 1;      // index chunks of 128 keys in shared memory
   static constexpr int kTile = (D / 64) * kRegion;
-  static constexpr int kK = 0;
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kTile;
   static constexpr int kV = kK + kSK * kTile;
   static constexpr int kBar = kV + kSV * kTile;
   static constexpr int kNumBars = 1 + 2 * kSK + 2 * kSV + 4 + 4;
@@ -62,7 +63,7 @@ struct SparseCfg {
   static constexpr int kIdx = kMisc + 32;
   static constexpr int kBytes = kIdx + kRing * 128 * 4;
   static constexpr int kAlloc = kBytes + 1024;
-  static constexpr uint32_t kColS = 0, kColO = 256, kColP = 384, kColQ = 448;
+  static constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
 };
 
 template <int D, int kEpi>
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
   const int32_t* idxg = p.idx + (size_t(bh) * p.G + g) * size_t(p.K);
 
   if (tid == 0) {
-    mbar_init(q_full, 128);
+    mbar_init(q_full, kGather);
     for (int s = 0; s < SK; ++s) {
       mbar_init(k_full + s, kGather);
       mbar_init(k_empty + s, 1);
@@ -128,11 +129,11 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem + L::kColS, tO = tmem + L::kColO, tP = tmem + L::kColP, tQ = tmem + L::kColQ;
+  const uint32_t tS = tmem + L::kColS, tO = tmem + L::kColO, tP = tmem + L::kColP;
 
   if (warp < 4) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegSoftmax));
-    // ------------------------------------------------------------ Q -> TMEM, softmax, epilogue
+    // ------------------------------------------------------------ softmax, epilogue
     const int row = tid;
     const uint32_t lane_off = uint32_t(warp * 32) << 16;
     int tok = -1;
@@ -140,29 +141,6 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
       const int v = __ldg(p.perm + size_t(bh) * p.N_pad + size_t(g) * p.C + row);
       if (v < 0 || v >= p.N_pad) raise_status(st, kStatusBounds);
       else if (v < p.N) tok = v;
-    }
-    {
-      // a bf16 row is already laid out as the packed pairs a TMEM column holds
-      uint32_t qw[64];
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + (size_t(bh) * p.N + size_t(tok < 0 ? 0 : tok)) * D);
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const uint4 v = tok >= 0 ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-        qw[4 * c] = v.x;
-        qw[4 * c + 1] = v.y;
-        qw[4 * c + 2] = v.z;
-        qw[4 * c + 3] = v.w;
-      }
-      if constexpr (D == 128) {
-        tmem_st64(tQ + lane_off, qw);
-      } else {
-        uint32_t q32[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) q32[i] = qw[i];
-        tmem_st32(tQ + lane_off, q32);
-      }
-      tc_fence_before();
-      mbar_arrive(q_full);
     }
     float m, l;
     const SoftmaxSync sy{s_full, s_free, p_full, p_empty};
@@ -182,6 +160,21 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
     const int ch = t % kChunks, r0 = t / kChunks;
     const __nv_bfloat16* kb = p.k + size_t(bh) * p.N * D;
     const __nv_bfloat16* vb = p.v + size_t(bh) * p.N * D;
+    {  // the group's query rows (through perm): operand A of S = Q K^T
+      const __nv_bfloat16* qb = p.q + size_t(bh) * p.N * D;
+      const int32_t* permg = p.perm + size_t(bh) * p.N_pad + size_t(g) * p.C;
+#pragma unroll 4
+      for (int it = 0; it < kPasses; ++it) {
+        const int row = it * kRowsPerPass + r0;
+        int tq = -1;
+        if (row < p.C) {
+          const int v = __ldg(permg + row);
+          if (v < 0 || v >= p.N_pad) raise_status(st, kStatusBounds);
+          else if (v < p.N) tq = v;
+        }
+        cp_async16(sbase + L::kQ + sw128_off(row, ch), qb + size_t(tq < 0 ? 0 : tq) * D + ch * 8, tq >= 0);
+      }
+    }
     // index chunks of tiles 0..kLag-1
 #pragma unroll
     for (int tt = 0; tt < kLag; ++tt)
@@ -191,6 +184,8 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
       }
     cp_async_commit();
     cp_async_wait<0>();
+    fence_proxy_async_smem();
+    mbar_arrive(q_full);
     named_bar_sync(1, kGather);
     int prev[kPasses];  // this thread's key ids of tile i-1, for its value rows
 #pragma unroll
@@ -284,7 +279,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
         const uint32_t kt = sbase + L::kK + (j % SK) * L::kTile;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          tc_mma_ts(tS + (j & 1) * 128, tQ + ks * 8, desc_kmajor(kt, ks), kIdescQK, ks > 0 ? 1u : 0u);
+          tc_mma_ss(tS + (j & 1) * 128, desc_kmajor(sbase + L::kQ, ks), desc_kmajor(kt, ks), kIdescQK, ks > 0 ? 1u : 0u);
         tc_commit(s_full + (j & 1));
         tc_commit(k_empty + j % SK);
         issued = true;
