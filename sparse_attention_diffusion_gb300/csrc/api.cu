@@ -257,6 +257,7 @@ mcs_status mcs_anchor_select(const mcs_desc* desc, const void* q, const void* k,
       p.perm = perm;
       p.lse = lse;
       p.scores = scores;
+      p.BH = dm.BH;
       p.N = dm.N;
       p.N_pad = dm.N_pad;
       p.C = dm.C;

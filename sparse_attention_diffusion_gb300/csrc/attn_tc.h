@@ -28,7 +28,7 @@ struct TcColsumParams {
   const int32_t* perm;          // [BH, N_pad]
   const float* lse;             // [BH, N]
   float* scores;                // [nrows, N] fp32 rows of this launch
-  int N, N_pad, C, G;
+  int BH, N, N_pad, C, G;
   int row0;                     // first group row (bh * G + g) of this launch
   float scale_log2;
   uint32_t* status;

@@ -1,0 +1,235 @@
+// Pass 2 of the anchor selection on the tcgen05 tensor cores, bf16 inputs
+// (sm_103a): for one query group g, the summed softmax weight of every key,
+//     S_g[j] = sum over the group's real queries i of exp(scale q_i.k_j - lse_i),
+// with lse from pass 1 (the dense kernel) [MC-Sparse summary: anchor two-pass
+// paragraph: the extra QK pass recomputes the probabilities].
+//
+// One CTA per group, 192 threads:
+//   warps 0-3   gather the group's query rows (through perm) once, then per key
+//               tile read the transposed logits S^T = K_tile Q_g^T from tensor
+//               memory: the TMEM lane is the key, so each thread sums its key's
+//               exp over the group's queries with no cross-thread reduction, and
+//               writes the key's score (consecutive threads, consecutive keys);
+//   warp 4      tensor-memory allocation and the single MMA-issuing thread; four
+//               (C = 128) or eight (C = 64) S^T buffers let it run ahead;
+//   warp 5      TMA producer: key tiles of 128 rows as tiled boxes of a 3-D
+//               tensor map into a 6-stage (d = 128) ring; rows >= N read zeros.
+// All waits are bounded; on a timeout the CTA flags it, lets its copies and
+// MMAs land, frees tensor memory and returns.
+#include "attn_tc.h"
+#include "common.cuh"
+#include "ptx.cuh"
+#include "tc_common.cuh"
+#include "tma.cuh"
+
+namespace mcs {
+namespace {
+
+constexpr int kColThreads = 192;
+
+template <int D, int CQ>
+struct ColCfg {
+  static constexpr int kStages = (D == 128) ? 6 : 10;  // key tiles of 128 rows
+  static constexpr int kTile = (D / 64) * kRegion;
+  static constexpr int kQ = 0;  // [CQ x D] (regions of 128 rows)
+  static constexpr int kK = kQ + kTile;
+  static constexpr int kBar = kK + kStages * kTile;
+  static constexpr int kNumBuf = 512 / CQ;  // S^T buffers of CQ columns
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 * kNumBuf + 1;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kLse = kMisc + 16;  // [128] fp32: -lse_i * log2(e), -inf for pads
+  static constexpr int kBytes = kLse + 128 * 4;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+template <int D, int CQ>
+__global__ void __launch_bounds__(kColThreads, 1)
+    colsum_kernel(const __grid_constant__ CUtensorMap map_k, const TcColsumParams p) {
+  using L = ColCfg<D, CQ>;
+  constexpr int S = L::kStages, NB = L::kNumBuf;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + S;
+  uint64_t* s_full = k_empty + S;  // [NB]
+  uint64_t* s_free = s_full + NB;  // [NB]
+  uint64_t* drain = s_free + NB;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  float* nlse = reinterpret_cast<float*>(smem + L::kLse);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int grow = p.row0 + blockIdx.x;  // global group row = bh * G + g
+  const int bh = grow / p.G, g = grow % p.G;
+  const int T = (p.N + 127) / 128;
+  uint32_t* st = p.status;
+
+  if (tid == 0) {
+    mbar_init(q_full, 128);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(k_full + s, 1);
+      mbar_init(k_empty + s, 1);
+    }
+    for (int b = 0; b < NB; ++b) {
+      mbar_init(s_full + b, 1);
+      mbar_init(s_free + b, 128);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    // ------------------------------------------------------------ query rows, then column sums
+    const int32_t* permg = p.perm + size_t(bh) * p.N_pad + size_t(g) * p.C;
+    {
+      constexpr int kChunks = D / 8, kRowsPerPass = 128 / kChunks;
+      const int ch = tid % kChunks, r0 = tid / kChunks;
+      const __nv_bfloat16* qb = p.q + size_t(bh) * p.N * D;
+#pragma unroll 4
+      for (int it = 0; it < CQ / kRowsPerPass; ++it) {
+        const int row = it * kRowsPerPass + r0;
+        int t = -1;
+        if (row < p.C) {
+          const int v = __ldg(permg + row);
+          if (v < 0 || v >= p.N_pad) raise_status(st, kStatusBounds);
+          else if (v < p.N) t = v;
+        }
+        cp_async16(sbase + L::kQ + sw128_off(row, ch), qb + size_t(t < 0 ? 0 : t) * D + ch * 8, t >= 0);
+      }
+      cp_async_commit();
+      if (tid < CQ) {
+        int t = -1;
+        if (tid < p.C) {
+          const int v = __ldg(permg + tid);
+          if (v >= 0 && v < p.N) t = v;
+        }
+        nlse[tid] = t >= 0 ? -__ldg(p.lse + size_t(bh) * p.N + t) * kLog2e : -INFINITY;
+      }
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      mbar_arrive(q_full);
+      named_bar_sync(2, 128);  // nlse visible to all column threads
+    }
+    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    float* out = p.scores + size_t(blockIdx.x) * p.N;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+      const int b = j % NB;
+      if (!warp_all(mbar_wait(s_full + b, uint32_t(j / NB) & 1, st))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c0 = 0; c0 < CQ; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + b * CQ + c0, r);
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 nl = *reinterpret_cast<const float4*>(nlse + c0 + i);
+          acc[0] += ex2_approx(fmaf(__uint_as_float(r[i]), sl2, nl.x));
+          acc[1] += ex2_approx(fmaf(__uint_as_float(r[i + 1]), sl2, nl.y));
+          acc[2] += ex2_approx(fmaf(__uint_as_float(r[i + 2]), sl2, nl.z));
+          acc[3] += ex2_approx(fmaf(__uint_as_float(r[i + 3]), sl2, nl.w));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(s_free + b);
+      const int key = j * 128 + tid;
+      if (key < p.N) out[key] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    }
+    if (!ok && tid == 0) raise_status(st, kStatusTimeout);
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ TMA producer
+    int armed = 0;
+    if (lane == 0) {
+      tma_prefetch_map(&map_k);
+      for (int j = 0; j < T; ++j) {
+        const int s = j % S;
+        if (!mbar_wait(k_empty + s, (uint32_t(j / S) & 1) ^ 1, st)) {
+          raise_status(st, kStatusTimeout);
+          break;
+        }
+        mbar_arrive_expect_tx(k_full + s, L::kTile);
+#pragma unroll
+        for (int rg = 0; rg < D / 64; ++rg)
+          tma_load_3d(sbase + L::kK + s * L::kTile + rg * kRegion, &map_k, rg * 64, j * 128, bh,
+                      smem_u32(k_full + s));
+        armed = j + 1;
+      }
+      // let every armed copy land before the CTA can exit
+      for (int t = (armed > S ? armed - S : 0); t < armed; ++t) mbar_wait(k_full + t % S, (t / S) & 1, st);
+    }
+    __syncwarp();
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdesc = idesc_bf16_f32(128, CQ, 0, 0);
+      bool ok = mbar_wait(q_full, 0, st);
+      bool issued = false;
+      for (int j = 0; ok && j < T; ++j) {
+        const int s = j % S, b = j % NB;
+        ok = mbar_wait(k_full + s, uint32_t(j / S) & 1, st) && mbar_wait(s_free + b, (uint32_t(j / NB) & 1) ^ 1, st);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t kt = sbase + L::kK + s * L::kTile;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          tc_mma_ss(tmem + b * CQ, desc_kmajor(kt, ks), desc_kmajor(sbase + L::kQ, ks), kIdesc, ks > 0 ? 1u : 0u);
+        tc_commit(s_full + b);
+        tc_commit(k_empty + s);
+        issued = true;
+      }
+      if (!ok) {
+        raise_status(st, kStatusTimeout);
+        if (issued) {
+          tc_commit(drain);
+          mbar_wait(drain, 0, st);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, int CQ>
+cudaError_t launch_colsum(const TcColsumParams& p, int nrows, cudaStream_t stream) {
+  using L = ColCfg<D, CQ>;
+  CUtensorMap mk;
+  if (!make_tile_map(&mk, p.k, p.BH, p.N, D, 128)) return cudaErrorInvalidValue;
+  auto kern = colsum_kernel<D, CQ>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  kern<<<nrows, kColThreads, L::kAlloc, stream>>>(mk, p);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t tc_colsum(int D, int C, const TcColsumParams& p, int nrows, cudaStream_t stream) {
+  if (D == 128 && C == 128) return launch_colsum<128, 128>(p, nrows, stream);
+  if (D == 128 && C == 64) return launch_colsum<128, 64>(p, nrows, stream);
+  if (D == 64 && C == 128) return launch_colsum<64, 128>(p, nrows, stream);
+  if (D == 64 && C == 64) return launch_colsum<64, 64>(p, nrows, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mcs

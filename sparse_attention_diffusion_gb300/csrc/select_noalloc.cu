@@ -84,6 +84,7 @@ extern "C" mcs_status mcs_anchor_select_noalloc(const mcs_desc* desc, const void
       p.perm = perm;
       p.lse = lse;
       p.scores = scores;
+      p.BH = static_cast<int>(BH);
       p.N = static_cast<int>(N);
       p.N_pad = static_cast<int>(G * C);
       p.C = static_cast<int>(C);
