@@ -52,8 +52,8 @@ __device__ __forceinline__ bool softmax_rows(int T, int nkv, uint32_t tS, uint32
 #pragma unroll
     for (int i = 0; i < 8; ++i) mp[i] = __uint_as_float(r[i]);
 #pragma unroll
-    for (int c = 8; c < 128; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(r[c]));
-    const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+    for (int c = 8; c < 128; c += 2) mp[(c >> 1) & 7] = fmax3(mp[(c >> 1) & 7], __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+    const float mx = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
     const float m_new = fmaxf(m, mx * sl2);
     const bool need = m_new > m + 8.f;
     const float m_use = need ? m_new : m;
