@@ -168,10 +168,10 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         if (!mbar_wait(v_full + s, u & 1, st)) return false;
         if (!mbar_wait(p_full, uint32_t(i) & 1, st)) return false;
         tc_fence_after();
-        const uint32_t vb = sbase + L::kV + s * L::kTile;
+        const uint32_t vlo = desc_lo_mnmajor(sbase + L::kV + s * L::kTile);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          tc_mma_ts(tO, tP + ks * 8, desc_mnmajor(vb, ks), kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
+          tc_mma_ts_lo(tO, tP + ks * 8, vlo + kstep_mnmajor(ks), kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
         tc_commit(p_empty);
         tc_commit(v_empty + s);
         return true;
@@ -182,10 +182,10 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         ok = mbar_wait(k_full + s, u & 1, st) && mbar_wait(s_free + b, (ub & 1) ^ 1, st);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t kb = sbase + L::kK + s * L::kTile;
+        const uint32_t klo = desc_lo_kmajor(sbase + L::kK + s * L::kTile), qlo = desc_lo_kmajor(sbase + L::kQ);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          tc_mma_ss(tS + b * 128, desc_kmajor(sbase + L::kQ, ks), desc_kmajor(kb, ks), kIdescQK, ks > 0 ? 1u : 0u);
+          tc_mma_ss_lo(tS + b * 128, qlo + kstep_kmajor(ks), klo + kstep_kmajor(ks), kIdescQK, ks > 0 ? 1u : 0u);
         tc_commit(s_full + b);
         tc_commit(k_empty + s);
         issued = true;

@@ -6,34 +6,39 @@
 // residual (reuse step) or store R = O_dense - O_sparse (anchor step)
 // [MC-Sparse summary: residual paragraph].
 //
-// One CTA per group, 512 threads in four warpgroups:
-//   warpgroup 0 (warps 0-3)   softmax, one thread per query row, and the epilogue;
-//   warpgroups 1-2 (4-11)     eight gather warps: the group's query rows (through
-//                             perm) once, then per iteration i the key rows of
-//                             tile i and the value rows of tile i-1 (128 keys per
-//                             tile) at the group's index list, as 16-byte cp.async
-//                             copies into a 3-stage K ring and a 3-stage V ring
-//                             (128-byte swizzled); the index list streams through
-//                             a shared-memory ring two tiles ahead;
-//   warpgroup 3 (warp 12)     tensor-memory allocation and the single
-//                             MMA-issuing thread (warps 13-15 idle).
-// A K stage is released when S of its tile is done, a V stage when PV is done,
-// so key rows are fetched well ahead of their use; iteration i's copies form one
-// cp.async group, retired (waited, proxy-fenced, arrived on the full barriers)
-// two iterations later. Each gather thread reads its row indices into registers
-// before issuing its copies back to back (a load between two copies would
-// serialise the warp on its latency) and keeps them for the value rows of the
-// same tile one iteration later. The MMA thread issues P_j V_j as soon as P_j is
-// written and only puts S_{j+1} first when its key rows have already landed.
-// Row gathers of 128-byte segments are kept on the load/store path: on this GPU
-// they move far more bytes per cycle than 4-row TMA gathers, and their
-// throughput grows with the number of issuing warps. Registers are rebalanced
-// with setmaxnreg (softmax 224, gather 80, MMA 64); the launcher checks that the
-// split fits the registers the block is launched with.
-// S = Q K^T reads both operands from shared memory; PV reads P from tensor memory.
-// Tensor memory: S0 [0,128), S1 [128,256), O [256,256+D), P [384,448).
-// All waits are bounded; on a timeout the CTA flags it, lets its copies and
-// MMAs land, frees tensor memory and returns.
+// One CTA per group (kernels that hold tensor memory run one CTA per SM). The
+// key tiles of 128 keys are split between two softmax warpgroups (even tiles,
+// odd tiles), each with its own S/P and O accumulators in tensor memory, so the
+// tensor core works for one warpgroup while the other computes exponentials;
+// the two partial softmaxes are merged in the epilogue (max, rescale, sum).
+// 640 threads in five warpgroups:
+//   warpgroups 0-1 (warps 0-7)    softmax of even / odd tiles, one thread per
+//                                 query row; the merged epilogue (each
+//                                 warpgroup stores half of the columns);
+//   warpgroups 2-3 (warps 8-15)   eight gather warps: the group's query rows
+//                                 (through perm) once, then per tile the key
+//                                 and value rows at the group's index list, as
+//                                 16-byte cp.async copies into 3-stage K and V
+//                                 rings (128-byte swizzled);
+//   warpgroup 4 (warp 16)         tensor-memory allocation and the single
+//                                 MMA-issuing thread (warps 17-19 idle).
+// The gather warps never wait for their own copies: each thread ends a tile's
+// key (value) copies with an asynchronous arrive on the stage's full barrier,
+// which completes when every thread's rows have landed; the MMA thread then
+// fences the generic-to-async proxy before the tensor core reads them. The
+// gather warps only wait (through one leader and a named barrier) for the
+// stages to be released: a K stage when S of its tile is done, a V stage when
+// PV is done. Each gather thread reads its row indices for the next tile into
+// registers while the leader waits, and issues a tile's copies back to back.
+// The MMA thread polls its barriers and issues whichever of S_j (into the S
+// buffer of warpgroup j%2, after P_{j-2} V_{j-2}: P is written over S) and
+// P_j V_j can go, in tile order for each kind.
+// Tensor memory: S/P of warpgroup w at [128w, 128w+128) (P in the first 64
+// columns), O of warpgroup w at [256 + wD, 256 + wD + D).
+// Registers are rebalanced with setmaxnreg (softmax 176, gather 48, warpgroup 4
+// 32); the launcher checks that the split fits the registers the block is
+// launched with. All waits are bounded; on a timeout the CTA flags it, lets its
+// copies and MMAs land, frees tensor memory and returns.
 #include "attn_common.cuh"
 #include "attn_tc.h"
 #include "common.cuh"
@@ -43,33 +48,33 @@
 namespace mcs {
 namespace {
 
-constexpr int kSparseThreads = 512;
-constexpr int kGather = 256;  // gather threads (warpgroups 1-2)
-constexpr int kRegSoftmax = 224, kRegGather = 80, kRegMma = 64;
-constexpr int kRegPool = 128 * kRegSoftmax + kGather * kRegGather + 128 * kRegMma;
+constexpr int kSparseThreads = 640;
+constexpr int kGather = 256;   // gather threads (warpgroups 2-3)
+constexpr int kMmaWarp = 16;   // first warp of warpgroup 4
+constexpr int kRegSoftmax = 176, kRegGather = 48, kRegMma = 32;
+constexpr int kRegPool = 256 * kRegSoftmax + kGather * kRegGather + 128 * kRegMma;
 
 template <int D>
 struct SparseCfg {
-  static constexpr int kSK = 3, kSV = 3;      // K and V stages
-  static constexpr int kLag = 2;              // iterations between a copy group's issue and its retirement
-  static constexpr int kRing = kLag + 1;      // index chunks of 128 keys in shared memory
+  static constexpr int kSK = 3, kSV = 3;      // K and V stages (equal: tile i's key and value rows go together)
   static constexpr int kTile = (D / 64) * kRegion;
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTile;
   static constexpr int kV = kK + kSK * kTile;
   static constexpr int kBar = kV + kSV * kTile;
-  static constexpr int kNumBars = 1 + 2 * kSK + 2 * kSV + 4 + 4;
+  static constexpr int kNumBars = 1 + 2 * kSK + 2 * kSV + 2 + 2 + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;  // tmem slot, stop flags [2]
-  static constexpr int kIdx = kMisc + 32;
-  static constexpr int kBytes = kIdx + kRing * 128 * 4;
+  static constexpr int kBytes = kMisc + 32;
   static constexpr int kAlloc = kBytes + 1024;
-  static constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+  static constexpr uint32_t kColO = 256;
+  static_assert(kAlloc <= 227 * 1024, "shared memory");
 };
 
 template <int D, int kEpi>
 __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const TcAttnParams p) {
   using L = SparseCfg<D>;
-  constexpr int SK = L::kSK, SV = L::kSV, kLag = L::kLag;
+  constexpr int SK = L::kSK, SV = L::kSV;
+  static_assert(SK == SV, "one stage index for tile i's key and value rows");
   constexpr int kChunks = D / 8;  // 16-byte chunks per row
   constexpr int kRowsPerPass = kGather / kChunks;
   constexpr int kPasses = 128 / kRowsPerPass;
@@ -82,17 +87,14 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
   uint64_t* k_empty = k_full + SK;
   uint64_t* v_full = k_empty + SK;
   uint64_t* v_empty = v_full + SV;
-  uint64_t* s_full = v_empty + SV;  // [2]
-  uint64_t* s_free = s_full + 2;    // [2]
-  uint64_t* p_full = s_free + 2;
-  uint64_t* p_empty = p_full + 1;
-  uint64_t* o_done = p_empty + 1;
+  uint64_t* s_full = v_empty + SV;  // [2] per warpgroup
+  uint64_t* p_full = s_full + 2;    // [2]
+  uint64_t* o_done = p_full + 2;
   uint64_t* drain = o_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   // the gather leader's decision for iteration i lives in stop[i & 1]: a slow
   // reader of iteration i never sees the leader's write for iteration i + 1
   volatile int* stop = reinterpret_cast<volatile int*>(smem + L::kMisc + 8);
-  int32_t* ring = reinterpret_cast<int32_t*>(smem + L::kIdx);  // [kRing][128]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.y, g = blockIdx.x;
@@ -111,17 +113,15 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
       mbar_init(v_full + s, kGather);
       mbar_init(v_empty + s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(s_full + b, 1);
-      mbar_init(s_free + b, 128);
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(s_full + w, 1);
+      mbar_init(p_full + w, 128);
     }
-    mbar_init(p_full, 128);
-    mbar_init(p_empty, 1);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     fence_mbar_init();
   }
-  if (warp == 12) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -129,13 +129,14 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem + L::kColS, tO = tmem + L::kColO, tP = tmem + L::kColP;
 
-  if (warp < 4) {
+  if (warp < 8) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegSoftmax));
     // ------------------------------------------------------------ softmax, epilogue
-    const int row = tid;
-    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    const int w = warp >> 2;  // warpgroup: tiles w, w + 2, ...
+    const int row = tid & 127;
+    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + uint32_t(w * 128), tO = tmem + L::kColO + uint32_t(w * D);
     int tok = -1;
     if (row < p.C) {
       const int v = __ldg(p.perm + size_t(bh) * p.N_pad + size_t(g) * p.C + row);
@@ -143,20 +144,36 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
       else if (v < p.N) tok = v;
     }
     float m, l;
-    const SoftmaxSync sy{s_full, s_free, p_full, p_empty};
-    bool ok = softmax_rows<D, true>(T, nkv, tS, tO, tP, lane_off, p.scale_log2, sy, st, m, l);
+    bool ok = softmax_rows_pp<D>(w, T, nkv, tS, tO, lane_off, p.scale_log2, s_full + w, p_full + w, st, m, l);
     if (ok) ok = warp_all(mbar_wait(o_done, 0, st));
+    // Both warpgroups must reach the exchange barrier, so a failed wait only
+    // skips the stores. After o_done every MMA has completed and every copy has
+    // landed, so the first K stage holds the two warpgroups' (m, l) per row.
+    float2* ml = reinterpret_cast<float2*>(smem + L::kK);  // [2][128]
+    fence_proxy_async_smem();
+    ml[w * 128 + row] = make_float2(m, l);
+    named_bar_sync(2, 256);
+    const float2 other = ml[(w ^ 1) * 128 + row];
+    const float m0 = w == 0 ? m : other.x, l0 = w == 0 ? l : other.y;
+    const float m1 = w == 0 ? other.x : m, l1 = w == 0 ? other.y : l;
+    const float mm = fmaxf(m0, m1);
+    const float f0 = ex2_approx(m0 - mm), f1 = T > 1 ? ex2_approx(m1 - mm) : 0.f;
+    const float inv = 1.f / (l0 * f0 + l1 * f1);
     if (ok) {
       tc_fence_after();
       __nv_bfloat16* dst = (kEpi == kEpiStoreResidual) ? p.res_out : p.o;
-      store_row<D, kEpi>(tO, lane_off, tok, (size_t(bh) * p.N + size_t(tok < 0 ? 0 : tok)) * D, 1.f / l, dst,
-                         p.res_in);
+      const size_t rowoff = (size_t(bh) * p.N + size_t(tok < 0 ? 0 : tok)) * D;
+      const uint32_t tO0 = tmem + L::kColO, tO1 = tmem + L::kColO + D;
+      if (w == 0)
+        store_row_merged<kEpi, 0, D / 2>(tO0, tO1, T > 1, lane_off, tok, rowoff, f0 * inv, f1 * inv, dst, p.res_in);
+      else
+        store_row_merged<kEpi, D / 2, D>(tO0, tO1, T > 1, lane_off, tok, rowoff, f0 * inv, f1 * inv, dst, p.res_in);
     }
     if (!ok && row == 0) raise_status(st, kStatusTimeout);
-  } else if (warp < 12) {
+  } else if (warp < 16) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegGather));
     // ------------------------------------------------------------ gather warps
-    const int t = tid - 128;  // 0..255
+    const int t = tid - 256;  // 0..255
     const int ch = t % kChunks, r0 = t / kChunks;
     const __nv_bfloat16* kb = p.k + size_t(bh) * p.N * D;
     const __nv_bfloat16* vb = p.v + size_t(bh) * p.N * D;
@@ -174,37 +191,28 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
         }
         cp_async16(sbase + L::kQ + sw128_off(row, ch), qb + size_t(tq < 0 ? 0 : tq) * D + ch * 8, tq >= 0);
       }
+      cp_async_arrive_noinc(q_full);
     }
-    // index chunks of tiles 0..kLag-1
+    // this thread's key ids of one tile (its rows r0 + k * kRowsPerPass); -1
+    // past the end of the list. Read one tile ahead, so the loads complete while
+    // the leader waits for the stages.
+    auto load_ids = [&](int i, int (&ids)[kPasses]) {
 #pragma unroll
-    for (int tt = 0; tt < kLag; ++tt)
-      for (int e = t; e < 128; e += kGather) {
-        const int slot = tt * 128 + e;
-        cp_async4(smem_u32(ring + tt * 128 + e), idxg + (slot < nkv ? slot : 0), slot < nkv);
+      for (int it = 0; it < kPasses; ++it) {
+        const int slot = i * 128 + it * kRowsPerPass + r0;
+        ids[it] = slot < nkv ? __ldg(idxg + slot) : -1;
       }
-    cp_async_commit();
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    mbar_arrive(q_full);
-    named_bar_sync(1, kGather);
-    int prev[kPasses];  // this thread's key ids of tile i-1, for its value rows
-#pragma unroll
-    for (int it = 0; it < kPasses; ++it) prev[it] = -1;
+    };
+    int cur[kPasses], nxt[kPasses];
+    load_ids(0, cur);
     bool ok = true;
-    int issued = 0;  // iterations whose copy group was committed
-    for (int i = 0; i <= T; ++i) {
-      if (i >= kLag) {  // retire iteration i - kLag: K of tile i-kLag, V of tile i-kLag-1
-        cp_async_wait<kLag - 1>();
-        fence_proxy_async_smem();
-        const int r = i - kLag;
-        if (r < T) mbar_arrive(k_full + r % SK);
-        if (r >= 1) mbar_arrive(v_full + (r - 1) % SV);
-      }
-      if (t == 0) {
+    for (int i = 0; i < T; ++i) {
+      if (i + 1 < T) load_ids(i + 1, nxt);
+      const int s = i % SK;
+      const uint32_t par = (uint32_t(i / SK) & 1) ^ 1;
+      if (t == 0) {  // the K stage (S of tile i-SK) and the V stage (PV of tile i-SV) are free
         int stp = 0;
-        if (i < T && !mbar_wait(k_empty + i % SK, ((i / SK) & 1) ^ 1, st)) stp = 1;           // S of tile i-SK done
-        if (!stp && i >= 1 && !mbar_wait(v_empty + (i - 1) % SV, (((i - 1) / SV) & 1) ^ 1, st))  // PV of tile i-1-SV
-          stp = 1;
+        if (!mbar_wait(k_empty + s, par, st) || !mbar_wait(v_empty + s, par, st)) stp = 1;
         if (stp) raise_status(st, kStatusTimeout);
         stop[i & 1] = stp;
       }
@@ -213,102 +221,90 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
         ok = false;
         break;
       }
-      int toks[kPasses];
-      if (i < T) {
-        const int32_t* rt = ring + (i % L::kRing) * 128;
 #pragma unroll
-        for (int it = 0; it < kPasses; ++it) {
-          const int row = it * kRowsPerPass + r0;
-          int tk = (i * 128 + row < nkv) ? rt[row] : -1;
-          if (tk >= p.N || (tk < 0 && i * 128 + row < nkv)) {
-            raise_status(st, kStatusBounds);
-            tk = -1;
-          }
-          toks[it] = tk;
-        }
-        const uint32_t dk = sbase + L::kK + (i % SK) * L::kTile;
-#pragma unroll
-        for (int it = 0; it < kPasses; ++it) {
-          const int row = it * kRowsPerPass + r0;
-          cp_async16(dk + sw128_off(row, ch), kb + size_t(toks[it] < 0 ? 0 : toks[it]) * D + ch * 8, toks[it] >= 0);
+      for (int it = 0; it < kPasses; ++it) {
+        const bool listed = i * 128 + it * kRowsPerPass + r0 < nkv;
+        if (cur[it] >= p.N || (cur[it] < 0 && listed)) {
+          raise_status(st, kStatusBounds);
+          cur[it] = -1;
         }
       }
-      if (i >= 1) {
-        const uint32_t dv = sbase + L::kV + ((i - 1) % SV) * L::kTile;
+      const uint32_t dk = sbase + L::kK + s * L::kTile, dv = sbase + L::kV + s * L::kTile;
 #pragma unroll
-        for (int it = 0; it < kPasses; ++it) {
-          const int row = it * kRowsPerPass + r0;
-          cp_async16(dv + sw128_off(row, ch), vb + size_t(prev[it] < 0 ? 0 : prev[it]) * D + ch * 8, prev[it] >= 0);
-        }
+      for (int it = 0; it < kPasses; ++it) {
+        const int row = it * kRowsPerPass + r0;
+        cp_async16(dk + sw128_off(row, ch), kb + size_t(cur[it] < 0 ? 0 : cur[it]) * D + ch * 8, cur[it] >= 0);
       }
-      for (int e = t; e < 128; e += kGather) {
-        const int tn = i + kLag, slot = tn * 128 + e;
-        cp_async4(smem_u32(ring + (tn % L::kRing) * 128 + e), idxg + (slot < nkv ? slot : 0), slot < nkv);
-      }
-      cp_async_commit();
-      issued = i + 1;
-      if (i < T) {
+      cp_async_arrive_noinc(k_full + s);
 #pragma unroll
-        for (int it = 0; it < kPasses; ++it) prev[it] = toks[it];
+      for (int it = 0; it < kPasses; ++it) {
+        const int row = it * kRowsPerPass + r0;
+        cp_async16(dv + sw128_off(row, ch), vb + size_t(cur[it] < 0 ? 0 : cur[it]) * D + ch * 8, cur[it] >= 0);
       }
+      cp_async_arrive_noinc(v_full + s);
+#pragma unroll
+      for (int it = 0; it < kPasses; ++it) cur[it] = nxt[it];
     }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    if (ok) {  // iterations issued - kLag .. issued - 1 were not retired in the loop
-      for (int r = (issued > kLag ? issued - kLag : 0); r < issued; ++r) {
-        if (r < T) mbar_arrive(k_full + r % SK);
-        if (r >= 1) mbar_arrive(v_full + (r - 1) % SV);
-      }
-    }
+    // let every copy land before the CTA can exit (normally long done)
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    (void)ok;
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegMma));
-    // ------------------------------------------------------------ MMA issuer (warp 12)
-    if (warp == 12 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (warp 16)
+    if (warp == kMmaWarp && lane == 0) {
       constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
       bool ok = mbar_wait(q_full, 0, st);
       bool issued = false;
-      if (ok) tc_fence_after();
-      auto s_ready = [&](int j) {
-        return mbar_test(k_full + j % SK, uint32_t(j / SK) & 1) && mbar_test(s_free + (j & 1), (uint32_t(j >> 1) & 1) ^ 1);
-      };
-      auto issue_s = [&](int j) -> bool {
-        if (!mbar_wait(k_full + j % SK, uint32_t(j / SK) & 1, st)) return false;
-        if (!mbar_wait(s_free + (j & 1), (uint32_t(j >> 1) & 1) ^ 1, st)) return false;
+      if (ok) {
+        fence_proxy_async_smem();  // rows written by the gather warps' cp.async copies
         tc_fence_after();
-        const uint32_t kt = sbase + L::kK + (j % SK) * L::kTile;
+      }
+      const uint32_t qlo = desc_lo_kmajor(sbase + L::kQ);
+      int ns = 0, np = 0;  // next S and next PV to issue
+      uint64_t t0 = 0;
+      for (uint32_t it = 0; ok && np < T; ++it) {
+        bool did = false;
+        // S_ns into the buffer of warpgroup ns%2 once its key rows are in and
+        // P_{ns-2} V_{ns-2}, which reads P from that buffer, has been issued: the
+        // MMAs of this thread run in issue order, so the PV reads P before S_ns
+        // overwrites it, and the commit that tells the softmax S_ns is done
+        // also covers that PV (O is stable when S_ns is seen)
+        if (ns < T && ns < np + 2 && mbar_test(k_full + ns % SK, uint32_t(ns / SK) & 1)) {
+          fence_proxy_async_smem();  // key rows landed by cp.async, read by the tensor core
+          tc_fence_after();
+          const uint32_t klo = desc_lo_kmajor(sbase + L::kK + (ns % SK) * L::kTile);
+          const uint32_t tS = tmem + uint32_t((ns & 1) * 128);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          tc_mma_ss(tS + (j & 1) * 128, desc_kmajor(sbase + L::kQ, ks), desc_kmajor(kt, ks), kIdescQK, ks > 0 ? 1u : 0u);
-        tc_commit(s_full + (j & 1));
-        tc_commit(k_empty + j % SK);
-        issued = true;
-        return true;
-      };
-      auto issue_pv = [&](int i) -> bool {
-        const int s = i % SV;
-        if (!mbar_wait(v_full + s, uint32_t(i / SV) & 1, st)) return false;
-        if (!mbar_wait(p_full, uint32_t(i) & 1, st)) return false;
-        tc_fence_after();
-        const uint32_t vt = sbase + L::kV + s * L::kTile;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          tc_mma_ts(tO, tP + ks * 8, desc_mnmajor(vt, ks), kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
-        tc_commit(p_empty);
-        tc_commit(v_empty + s);
-        return true;
-      };
-      if (ok && T > 0) ok = issue_s(0);
-      for (int j = 0; ok && j < T; ++j) {
-        // S_{j+1} and PV_j are independent: take S_{j+1} first only if it can go now
-        const bool s_next = j + 1 < T;
-        bool s_done = false;
-        if (s_next && s_ready(j + 1)) {
-          ok = issue_s(j + 1);
-          s_done = true;
+          for (int ks = 0; ks < D / 16; ++ks)
+            tc_mma_ss_lo(tS, qlo + kstep_kmajor(ks), klo + kstep_kmajor(ks), kIdescQK, ks > 0 ? 1u : 0u);
+          tc_commit(s_full + (ns & 1));
+          tc_commit(k_empty + ns % SK);
+          issued = true;
+          ++ns;
+          did = true;
         }
-        if (ok) ok = issue_pv(j);
-        if (ok && s_next && !s_done) ok = issue_s(j + 1);
+        // P_np V_np: P written by warpgroup np%2 and the value rows in
+        if (np < ns && mbar_test(p_full + (np & 1), uint32_t(np >> 1) & 1) &&
+            mbar_test(v_full + np % SV, uint32_t(np / SV) & 1)) {
+          fence_proxy_async_smem();  // value rows landed by cp.async
+          tc_fence_after();
+          const uint32_t vlo = desc_lo_mnmajor(sbase + L::kV + (np % SV) * L::kTile);
+          const uint32_t tP = tmem + uint32_t((np & 1) * 128), tO = tmem + L::kColO + uint32_t((np & 1) * D);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            tc_mma_ts_lo(tO, tP + ks * 8, vlo + kstep_mnmajor(ks), kIdescPV, (np >= 2 || ks > 0) ? 1u : 0u);
+          tc_commit(v_empty + np % SV);
+          ++np;
+          did = true;
+        }
+        if (did) {
+          t0 = 0;
+        } else if ((it & 255u) == 0) {  // nothing could go: bounded wait
+          const uint64_t now = globaltimer_ns();
+          if (t0 == 0) t0 = now;
+          else if (now - t0 > kWaitLimitNs || (peek_status(st) & kStatusTimeout)) ok = false;
+        }
       }
       if (ok) tc_commit(o_done);
       if (!ok) {
@@ -322,7 +318,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 12) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

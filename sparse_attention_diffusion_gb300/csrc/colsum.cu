@@ -184,10 +184,10 @@ __global__ void __launch_bounds__(kColThreads, 1)
         ok = mbar_wait(k_full + s, uint32_t(j / S) & 1, st) && mbar_wait(s_free + b, (uint32_t(j / NB) & 1) ^ 1, st);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t kt = sbase + L::kK + s * L::kTile;
+        const uint32_t klo = desc_lo_kmajor(sbase + L::kK + s * L::kTile), qlo = desc_lo_kmajor(sbase + L::kQ);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          tc_mma_ss(tmem + b * CQ, desc_kmajor(kt, ks), desc_kmajor(sbase + L::kQ, ks), kIdesc, ks > 0 ? 1u : 0u);
+          tc_mma_ss_lo(tmem + b * CQ, klo + kstep_kmajor(ks), qlo + kstep_kmajor(ks), kIdesc, ks > 0 ? 1u : 0u);
         tc_commit(s_full + b);
         tc_commit(k_empty + s);
         issued = true;

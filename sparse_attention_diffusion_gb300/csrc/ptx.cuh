@@ -82,6 +82,13 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool va
   const uint32_t n = valid ? 4u : 0u;
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
 }
+// Arrive (once, asynchronously) on an mbarrier when all of this thread's prior
+// cp.async copies have landed; .noinc: the arrival counts toward the barrier's
+// expected count, so a barrier fed this way is initialised with one count per
+// copying thread.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {

@@ -33,6 +33,42 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int s) {
   return smem_desc_sw128(base + uint32_t(s * 16 * 128), kRegion, 1024);
 }
 
+// Descriptor words for MMA issue loops. A step along K (K-major operand) or
+// along rows (MN-major operand) only moves the start address, which sits in the
+// low word and cannot carry out of its 14-bit field for shared-memory addresses,
+// so a loop keeps one base low word per operand and adds compile-time step
+// offsets; the high word (stride byte offset 1024, version, 128-byte swizzle) is
+// the same constant for every operand here. desc_kmajor(b, s) has the words
+// {desc_lo_kmajor(b) + kstep_kmajor(s), kDescHi}; desc_mnmajor likewise.
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t desc_lo_kmajor(uint32_t base) { return ((base >> 4) & 0x3FFFu) | (1u << 16); }
+__device__ __forceinline__ uint32_t desc_lo_mnmajor(uint32_t base) {
+  return ((base >> 4) & 0x3FFFu) | (uint32_t(kRegion >> 4) << 16);
+}
+__host__ __device__ constexpr uint32_t kstep_kmajor(int s) { return uint32_t((s >> 2) * (kRegion >> 4) + (s & 3) * 2); }
+__host__ __device__ constexpr uint32_t kstep_mnmajor(int s) { return uint32_t(s * 16 * 128 / 16); }
+
+// D[tmem] (+)= A[smem] * B[smem]^T from descriptor low words (high word kDescHi).
+__device__ __forceinline__ void tc_mma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 da, db;\n setp.ne.b32 p, %4, 0;\n"
+      " mov.b64 da, {%1, %5};\n mov.b64 db, {%2, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem] from the B descriptor's low word.
+__device__ __forceinline__ void tc_mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 db;\n setp.ne.b32 p, %4, 0;\n"
+      " mov.b64 db, {%2, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi)
+      : "memory");
+}
+
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
 }  // namespace mcs
