@@ -20,8 +20,9 @@
 //                                 and value rows at the group's index list, as
 //                                 16-byte cp.async copies into 3-stage K and V
 //                                 rings (128-byte swizzled);
-//   warpgroup 4 (warp 16)         tensor-memory allocation and the single
-//                                 MMA-issuing thread (warps 17-19 idle).
+//   warpgroup 4 (warp 16)         tensor-memory allocation and the MMA
+//                                 schedule, run by the whole warp with lane 0
+//                                 issuing (warps 17-19 idle).
 // The gather warps never wait for their own copies: each thread ends a tile's
 // key (value) copies with an asynchronous arrive on the stage's full barrier,
 // which completes when every thread's rows have landed; the MMA thread then
@@ -251,10 +252,13 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegMma));
     // ------------------------------------------------------------ MMA issuer (warp 16)
-    if (warp == kMmaWarp && lane == 0) {
+    // The whole warp runs the schedule, so every operand is warp-uniform (barrier
+    // tests are voted); lane 0 issues the MMAs and the commits.
+    if (warp == kMmaWarp) {
+      const bool leader = lane == 0;
       constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
-      bool ok = mbar_wait(q_full, 0, st);
+      bool ok = warp_all(mbar_wait(q_full, 0, st));
       bool issued = false;
       if (ok) {
         fence_proxy_async_smem();  // rows written by the gather warps' cp.async copies
@@ -270,31 +274,31 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
         // MMAs of this thread run in issue order, so the PV reads P before S_ns
         // overwrites it, and the commit that tells the softmax S_ns is done
         // also covers that PV (O is stable when S_ns is seen)
-        if (ns < T && ns < np + 2 && mbar_test(k_full + ns % SK, uint32_t(ns / SK) & 1)) {
+        if (ns < T && ns < np + 2 && warp_all(mbar_test(k_full + ns % SK, uint32_t(ns / SK) & 1))) {
           fence_proxy_async_smem();  // key rows landed by cp.async, read by the tensor core
           tc_fence_after();
           const uint32_t klo = desc_lo_kmajor(sbase + L::kK + (ns % SK) * L::kTile);
           const uint32_t tS = tmem + uint32_t((ns & 1) * 128);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks)
-            tc_mma_ss_lo(tS, qlo + kstep_kmajor(ks), klo + kstep_kmajor(ks), kIdescQK, ks > 0 ? 1u : 0u);
-          tc_commit(s_full + (ns & 1));
-          tc_commit(k_empty + ns % SK);
+            tc_mma_ss_lo_if(leader, tS, qlo + kstep_kmajor(ks), klo + kstep_kmajor(ks), kIdescQK, ks > 0 ? 1u : 0u);
+          tc_commit_if(leader, s_full + (ns & 1));
+          tc_commit_if(leader, k_empty + ns % SK);
           issued = true;
           ++ns;
           did = true;
         }
         // P_np V_np: P written by warpgroup np%2 and the value rows in
-        if (np < ns && mbar_test(p_full + (np & 1), uint32_t(np >> 1) & 1) &&
-            mbar_test(v_full + np % SV, uint32_t(np / SV) & 1)) {
+        if (np < ns && warp_all(mbar_test(p_full + (np & 1), uint32_t(np >> 1) & 1) &&
+                                mbar_test(v_full + np % SV, uint32_t(np / SV) & 1))) {
           fence_proxy_async_smem();  // value rows landed by cp.async
           tc_fence_after();
           const uint32_t vlo = desc_lo_mnmajor(sbase + L::kV + (np % SV) * L::kTile);
           const uint32_t tP = tmem + uint32_t((np & 1) * 128), tO = tmem + L::kColO + uint32_t((np & 1) * D);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc_mma_ts_lo(tO, tP + ks * 8, vlo + kstep_mnmajor(ks), kIdescPV, (np >= 2 || ks > 0) ? 1u : 0u);
-          tc_commit(v_empty + np % SV);
+            tc_mma_ts_lo_if(leader, tO, tP + ks * 8, vlo + kstep_mnmajor(ks), kIdescPV, (np >= 2 || ks > 0) ? 1u : 0u);
+          tc_commit_if(leader, v_empty + np % SV);
           ++np;
           did = true;
         }
@@ -304,13 +308,14 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
           const uint64_t now = globaltimer_ns();
           if (t0 == 0) t0 = now;
           else if (now - t0 > kWaitLimitNs || (peek_status(st) & kStatusTimeout)) ok = false;
+          ok = warp_all(ok);
         }
       }
-      if (ok) tc_commit(o_done);
+      if (ok) tc_commit_if(leader, o_done);
       if (!ok) {
-        raise_status(st, kStatusTimeout);
+        if (leader) raise_status(st, kStatusTimeout);
         if (issued) {
-          tc_commit(drain);
+          tc_commit_if(leader, drain);
           mbar_wait(drain, 0, st);
         }
       }

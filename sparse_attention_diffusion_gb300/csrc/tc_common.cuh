@@ -69,6 +69,35 @@ __device__ __forceinline__ void tc_mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// Warp-wide forms: every lane of the issuing warp executes the statement with
+// the same (warp-uniform) operands and only the lane with `issue` set issues the
+// MMA or the commit, so the operands can live in uniform registers.
+__device__ __forceinline__ void tc_mma_ss_lo_if(bool issue, uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n .reg .b64 da, db;\n setp.ne.b32 p, %4, 0;\n setp.ne.b32 q, %6, 0;\n"
+      " mov.b64 da, {%1, %5};\n mov.b64 db, {%2, %5};\n"
+      " @q tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi), "r"(uint32_t(issue))
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_ts_lo_if(bool issue, uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n .reg .b64 db;\n setp.ne.b32 p, %4, 0;\n setp.ne.b32 q, %6, 0;\n"
+      " mov.b64 db, {%2, %5};\n"
+      " @q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi), "r"(uint32_t(issue))
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_if(bool issue, uint64_t* bar) {
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.b32 q, %1, 0;\n"
+      " @q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(smem_u32(bar)),
+      "r"(uint32_t(issue))
+      : "memory");
+}
+
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
 }  // namespace mcs
