@@ -31,10 +31,11 @@ sys.path.insert(0, ROOT)
 METRIC = "sparse-attn ms/layer & TFLOP/s (frac of bf16 roofline) at density 0.15-0.25"
 UNIT = "ms/layer"
 REUSE_PER_STEP = 9
-# DRAM bytes (read + write) of one reuse-kernel launch on the 40-head layer: the
-# 8-head ncu capture (1.117 GB read + 0.149 GB write) scaled by heads; the summary is
-# profiles/attn_fwd_sparse_kernel-bench-720p-h8.md. Set to None when the kernel changes.
-SPARSE_TRAFFIC_BYTES_H40 = (1.117e9 + 0.149e9) * 40 / 8
+# DRAM bytes (read + write) of one reuse-kernel launch on the 40-head layer: an
+# 8-head ncu capture scaled by heads (traffic grows in proportion); the summary is
+# profiles/attn_sparse_kernel-kernel-bench-720p-h8.md (1.1405 GB read + 0.1620 GB
+# written per 8-head launch). Set to None when the kernel changes.
+SPARSE_TRAFFIC_BYTES_H40 = (1.1405e9 + 0.1620e9) * 40 / 8
 
 
 def parse():
@@ -306,8 +307,9 @@ def run_mcs(args, wl, K):
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
                          "frac": achieved / pk["bf16_sus"],
                          "traffic": (SPARSE_TRAFFIC_BYTES_H40 * wl.H / 40
-                                     if (wl.name == "kernel-bench-720p" and wl.d == 128 and K == 15120) else None),
-                         "kernel": "attn_fwd_kernel<128, sparse, add-residual>",
+                                     if (SPARSE_TRAFFIC_BYTES_H40 is not None and wl.name == "kernel-bench-720p"
+                                         and wl.d == 128 and K == 15120) else None),
+                         "kernel": "attn_sparse_kernel<128, add-residual>",
                          "peak_kind": f"{pk['src']} sustained bf16",
                          "algorithmic": "4*B*H*N*K*d kept FLOPs per launch"},
             "stages_ms": {s: statistics.mean(v) for s, v in stage_ms.items()},
