@@ -59,16 +59,21 @@ __device__ __forceinline__ bool softmax_rows(int T, int nkv, uint32_t tS, uint32
     const float m_use = need ? m_new : m;
     const float alpha = need ? ex2_approx(m - m_new) : 1.f;
     const float neg_m = -m_use;
-    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+    // two scores per packed FMA and two packed partial sums (four lanes)
+    const uint64_t sl2x2 = f2_pack(sl2, sl2), negmx2 = f2_pack(neg_m, neg_m);
+    uint64_t ls2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
     uint32_t pk[64];
 #pragma unroll
     for (int c = 0; c < 64; ++c) {
-      const float p0 = ex2_approx(fmaf(__uint_as_float(r[2 * c]), sl2, neg_m));
-      const float p1 = ex2_approx(fmaf(__uint_as_float(r[2 * c + 1]), sl2, neg_m));
-      ls[c & 3] += p0 + p1;
+      float x0, x1;
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])), sl2x2, negmx2), x0, x1);
+      const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+      ls2[c & 1] = f2_add(ls2[c & 1], f2_pack(p0, p1));
       pk[c] = pack_bf16x2(p0, p1);
     }
-    const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+    float la, lb;
+    f2_unpack(f2_add(ls2[0], ls2[1]), la, lb);
+    const float lsum = la + lb;
     l = l * alpha + lsum;
     m = m_use;
     if constexpr (kPV) {
@@ -133,16 +138,21 @@ __device__ __forceinline__ bool softmax_rows_pp(int j0, int T, int nkv, uint32_t
     const float m_use = need ? m_new : m;
     const float alpha = need ? ex2_approx(m - m_new) : 1.f;
     const float neg_m = -m_use;
-    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+    // two scores per packed FMA and two packed partial sums (four lanes)
+    const uint64_t sl2x2 = f2_pack(sl2, sl2), negmx2 = f2_pack(neg_m, neg_m);
+    uint64_t ls2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
     uint32_t pk[64];
 #pragma unroll
     for (int c = 0; c < 64; ++c) {
-      const float p0 = ex2_approx(fmaf(__uint_as_float(r[2 * c]), sl2, neg_m));
-      const float p1 = ex2_approx(fmaf(__uint_as_float(r[2 * c + 1]), sl2, neg_m));
-      ls[c & 3] += p0 + p1;
+      float x0, x1;
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])), sl2x2, negmx2), x0, x1);
+      const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+      ls2[c & 1] = f2_add(ls2[c & 1], f2_pack(p0, p1));
       pk[c] = pack_bf16x2(p0, p1);
     }
-    const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+    float la, lb;
+    f2_unpack(f2_add(ls2[0], ls2[1]), la, lb);
+    const float lsum = la + lb;
     l = l * alpha + lsum;
     m = m_use;
     if (__any_sync(0xffffffffu, need && n > 0)) {

@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
     const uint32_t lane_off = uint32_t(warp * 32) << 16;
     float* out = p.scores + size_t(blockIdx.x) * p.N;
     const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
     bool ok = true;
     for (int j = 0; j < T; ++j) {
       const int b = j % NB;
@@ -131,7 +132,8 @@ __global__ void __launch_bounds__(kColThreads, 1)
         break;
       }
       tc_fence_after();
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      // packed pairs: one FMA for two logits, two packed partial sums (four lanes)
+      uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
       for (int c0 = 0; c0 < CQ; c0 += 32) {
         uint32_t r[32];
@@ -139,16 +141,19 @@ __global__ void __launch_bounds__(kColThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
           const float4 nl = *reinterpret_cast<const float4*>(nlse + c0 + i);
-          acc[0] += ex2_approx(fmaf(__uint_as_float(r[i]), sl2, nl.x));
-          acc[1] += ex2_approx(fmaf(__uint_as_float(r[i + 1]), sl2, nl.y));
-          acc[2] += ex2_approx(fmaf(__uint_as_float(r[i + 2]), sl2, nl.z));
-          acc[3] += ex2_approx(fmaf(__uint_as_float(r[i + 3]), sl2, nl.w));
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), sl2x2, f2_pack(nl.x, nl.y)), x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])), sl2x2, f2_pack(nl.z, nl.w)), x2, x3);
+          acc2[0] = f2_add(acc2[0], f2_pack(ex2_approx(x0), ex2_approx(x1)));
+          acc2[1] = f2_add(acc2[1], f2_pack(ex2_approx(x2), ex2_approx(x3)));
         }
       }
       tc_fence_before();
       mbar_arrive(s_free + b);
       const int key = j * 128 + tid;
-      if (key < p.N) out[key] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+      float a0, a1;
+      f2_unpack(f2_add(acc2[0], acc2[1]), a0, a1);
+      if (key < p.N) out[key] = a0 + a1;
     }
     if (!ok && tid == 0) raise_status(st, kStatusTimeout);
   } else if (warp == 5) {
