@@ -194,9 +194,9 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
       }
       cp_async_arrive_noinc(q_full);
     }
-    // this thread's key ids of one tile (its rows r0 + k * kRowsPerPass); -1
-    // past the end of the list. Read one tile ahead, so the loads complete while
-    // the leader waits for the stages.
+    // This thread's key ids of tile i (its rows r0 + k * kRowsPerPass), -1 past
+    // the end of the list; read one tile ahead, so the loads complete while the
+    // leader waits for the stages.
     auto load_ids = [&](int i, int (&ids)[kPasses]) {
 #pragma unroll
       for (int it = 0; it < kPasses; ++it) {
@@ -204,11 +204,15 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
         ids[it] = slot < nkv ? __ldg(idxg + slot) : -1;
       }
     };
-    int cur[kPasses], nxt[kPasses];
-    load_ids(0, cur);
-    bool ok = true;
-    for (int i = 0; i < T; ++i) {
-      if (i + 1 < T) load_ids(i + 1, nxt);
+    static_assert(kRowsPerPass % 8 == 0, "a thread's rows share one swizzle phase");
+    const uint32_t doff = sw128_off(r0, ch);  // + it * kRowsPerPass * 128 for pass it
+    const __nv_bfloat16* kbc = kb + ch * 8;
+    const __nv_bfloat16* vbc = vb + ch * 8;
+    // one tile: wait for its stages, then key and value copies, each ended by an
+    // asynchronous arrive on the stage's full barrier. Listed ids outside [0, N)
+    // raise the bounds flag; they and the unlisted slots of the last tile read zeros.
+    auto tile = [&](int i, int (&ids)[kPasses], int (&next)[kPasses]) -> bool {
+      if (i + 1 < T) load_ids(i + 1, next);
       const int s = i % SK;
       const uint32_t par = (uint32_t(i / SK) & 1) ^ 1;
       if (t == 0) {  // the K stage (S of tile i-SK) and the V stage (PV of tile i-SV) are free
@@ -218,33 +222,46 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
         stop[i & 1] = stp;
       }
       named_bar_sync(1, kGather);
-      if (stop[i & 1]) {
-        ok = false;
-        break;
-      }
+      if (stop[i & 1]) return false;
+      bool all_valid = true;
 #pragma unroll
-      for (int it = 0; it < kPasses; ++it) {
-        const bool listed = i * 128 + it * kRowsPerPass + r0 < nkv;
-        if (cur[it] >= p.N || (cur[it] < 0 && listed)) {
-          raise_status(st, kStatusBounds);
-          cur[it] = -1;
+      for (int it = 0; it < kPasses; ++it) all_valid &= uint32_t(ids[it]) < uint32_t(p.N);
+      const uint32_t dk = sbase + L::kK + s * L::kTile + doff, dv = sbase + L::kV + s * L::kTile + doff;
+      if (all_valid) {
+#pragma unroll
+        for (int it = 0; it < kPasses; ++it)
+          cp_async16(dk + it * kRowsPerPass * 128, kbc + size_t(uint32_t(ids[it])) * D, true);
+        cp_async_arrive_noinc(k_full + s);
+#pragma unroll
+        for (int it = 0; it < kPasses; ++it)
+          cp_async16(dv + it * kRowsPerPass * 128, vbc + size_t(uint32_t(ids[it])) * D, true);
+        cp_async_arrive_noinc(v_full + s);
+      } else {
+#pragma unroll
+        for (int it = 0; it < kPasses; ++it) {
+          const bool listed = i * 128 + it * kRowsPerPass + r0 < nkv;
+          if (uint32_t(ids[it]) >= uint32_t(p.N)) {
+            if (listed) raise_status(st, kStatusBounds);
+            ids[it] = -1;
+          }
         }
-      }
-      const uint32_t dk = sbase + L::kK + s * L::kTile, dv = sbase + L::kV + s * L::kTile;
 #pragma unroll
-      for (int it = 0; it < kPasses; ++it) {
-        const int row = it * kRowsPerPass + r0;
-        cp_async16(dk + sw128_off(row, ch), kb + size_t(cur[it] < 0 ? 0 : cur[it]) * D + ch * 8, cur[it] >= 0);
-      }
-      cp_async_arrive_noinc(k_full + s);
+        for (int it = 0; it < kPasses; ++it)
+          cp_async16(dk + it * kRowsPerPass * 128, kbc + size_t(ids[it] < 0 ? 0 : ids[it]) * D, ids[it] >= 0);
+        cp_async_arrive_noinc(k_full + s);
 #pragma unroll
-      for (int it = 0; it < kPasses; ++it) {
-        const int row = it * kRowsPerPass + r0;
-        cp_async16(dv + sw128_off(row, ch), vb + size_t(cur[it] < 0 ? 0 : cur[it]) * D + ch * 8, cur[it] >= 0);
+        for (int it = 0; it < kPasses; ++it)
+          cp_async16(dv + it * kRowsPerPass * 128, vbc + size_t(ids[it] < 0 ? 0 : ids[it]) * D, ids[it] >= 0);
+        cp_async_arrive_noinc(v_full + s);
       }
-      cp_async_arrive_noinc(v_full + s);
-#pragma unroll
-      for (int it = 0; it < kPasses; ++it) cur[it] = nxt[it];
+      return true;
+    };
+    int ida[kPasses], idb[kPasses];  // ids of even / odd tiles (no copies between them)
+    load_ids(0, ida);
+    bool ok = true;
+    for (int i = 0; ok && i < T; i += 2) {
+      ok = tile(i, ida, idb);
+      if (ok && i + 1 < T) ok = tile(i + 1, idb, ida);
     }
     // let every copy land before the CTA can exit (normally long done)
     asm volatile("cp.async.wait_all;" ::: "memory");
