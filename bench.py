@@ -11,8 +11,12 @@ One step = one anchor period of the meta-cache schedule (anchor every 10 steps):
 Every kernel is timed with CUDA events on the launching stream. The headline
 value is the sparse attention layer time (ms/layer, lower is better) of the
 reuse kernel; the roofline object covers that kernel (kept FLOPs / time against
-the measured sustained bf16 peak). `--impl reference` times the float64 CPU
-oracle instead, on a bounded sample of groups, extrapolated to ms/layer.
+the measured sustained bf16 peak). After the timed steps (outside the timed
+region) the 118,800-token schedule (24 heads, 50 steps, densities 0.15 and 0.25)
+runs once to report the total time including anchors and the anchor overhead as
+equivalent extra density (`anchor_overhead`; `--no-schedule` skips it).
+`--impl reference` times the float64 CPU oracle instead, on a bounded sample of
+groups, extrapolated to ms/layer.
 """
 from __future__ import annotations
 
@@ -47,6 +51,7 @@ def parse():
     ap.add_argument("--workload", default="kernel-bench-720p")
     ap.add_argument("--density", default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-schedule", action="store_true", help="skip the 118,800-token schedule (anchor overhead)")
     ap.add_argument("--heads", type=int, default=None, help="override H (smaller case for profiler captures)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget (CPU seconds)")
     return ap.parse_args()
@@ -182,6 +187,39 @@ def run_reference(args, wl, K):
 
 
 # ---------------------------------------------------------------- GPU arm
+def schedule_overhead(dev):
+    """The full meta-cache schedule on the 118,800-token layer (24 heads, 50 steps:
+    5 dense warm-up steps, an anchor every 10 steps, reuse steps otherwise, drift
+    0.05) at densities 0.15 and 0.25: total time including anchors and the anchor
+    cost as equivalent extra density (post-warm-up time over 45 dense steps)."""
+    import torch
+
+    from sparse_attention_diffusion_gb300 import mcs, schedule, synth
+
+    out = {"workload": synth.SCHEDULE_HY.name, "steps": 50, "warmup": 5, "period": 10}
+    for rho in ("0.15", "0.25"):
+        wl = synth.SCHEDULE_HY.with_(density=rho)
+        layer = synth.make_layer(wl, device=dev)
+        q0, _, _ = layer.cast()
+        desc = mcs.desc_for(q0, wl.C)
+        ml = schedule.MetaCacheLayer(desc, wl.K, q0.dtype, dev)
+        del q0
+        recs = schedule.run(ml, schedule.Schedule(steps=50, warmup=5, period=10), layer.cast,
+                            lambda: layer.drift_step())
+        mcs.mcs_check_status()
+        t_dense = statistics.median(r.ms for r in recs[1:5])  # the first dense step pays one-off costs
+        rho_eq, extra = schedule.anchor_overhead(recs, t_dense, float(wl.density), 5)
+        kinds = {k: [r.ms for r in recs if r.kind == k] for k in ("dense", "anchor", "reuse")}
+        out[rho] = {"K": wl.K, "total_ms": sum(r.ms for r in recs), "post_warmup_ms": sum(r.ms for r in recs[5:]),
+                    "dense_step_ms": t_dense, "anchor_step_ms": statistics.mean(kinds["anchor"]),
+                    "reuse_step_ms": statistics.mean(kinds["reuse"]), "rho_eq": rho_eq,
+                    "anchor_overhead_points": 100.0 * extra,
+                    "vs_all_dense": 50 * t_dense / sum(r.ms for r in recs)}
+        del ml, layer, recs
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_mcs(args, wl, K):
     import torch
     import torch.distributed as dist
@@ -323,6 +361,8 @@ def run_mcs(args, wl, K):
                     "d2h_bytes_per_step": o.numel() * o.element_size()},
             "clocks": clocks,
         }
+        if world == 1 and not args.no_schedule:
+            line["anchor_overhead"] = schedule_overhead(dev)
         if world == 1 and not args.no_cpu_baseline:
             dt, g, thr = oracle_sample(wl, K, args.cpu_seconds)
             val = dt / g * wl.B * wl.H * wl.G * 1e3
