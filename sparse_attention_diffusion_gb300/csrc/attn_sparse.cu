@@ -31,9 +31,9 @@
 // stages to be released: a K stage when S of its tile is done, a V stage when
 // PV is done. Each gather thread reads its row indices for the next tile into
 // registers while the leader waits, and issues a tile's copies back to back.
-// The MMA thread polls its barriers and issues whichever of S_j (into the S
-// buffer of warpgroup j%2, after P_{j-2} V_{j-2}: P is written over S) and
-// P_j V_j can go, in tile order for each kind.
+// The MMA warp issues S_0, S_1, then P_j V_j followed by S_{j+2} (into the S
+// buffer of warpgroup j%2, whose first columns held P_j), waiting on each
+// operand's barrier in turn.
 // Tensor memory: S/P of warpgroup w at [128w, 128w+128) (P in the first 64
 // columns), O of warpgroup w at [256 + wD, 256 + wD + D).
 // Registers are rebalanced with setmaxnreg (softmax 176, gather 48, warpgroup 4
@@ -282,51 +282,45 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
         tc_fence_after();
       }
       const uint32_t qlo = desc_lo_kmajor(sbase + L::kQ);
-      int ns = 0, np = 0;  // next S and next PV to issue
-      uint64_t t0 = 0;
-      for (uint32_t it = 0; ok && np < T; ++it) {
-        bool did = false;
-        // S_ns into the buffer of warpgroup ns%2 once its key rows are in and
-        // P_{ns-2} V_{ns-2}, which reads P from that buffer, has been issued: the
-        // MMAs of this thread run in issue order, so the PV reads P before S_ns
-        // overwrites it, and the commit that tells the softmax S_ns is done
-        // also covers that PV (O is stable when S_ns is seen)
-        if (ns < T && ns < np + 2 && warp_all(mbar_test(k_full + ns % SK, uint32_t(ns / SK) & 1))) {
-          fence_proxy_async_smem();  // key rows landed by cp.async, read by the tensor core
-          tc_fence_after();
-          const uint32_t klo = desc_lo_kmajor(sbase + L::kK + (ns % SK) * L::kTile);
-          const uint32_t tS = tmem + uint32_t((ns & 1) * 128);
+      // Fixed issue order S_0, S_1, then P_j V_j followed by S_{j+2}: S_{j+2}
+      // writes the buffer that holds P_j, and the MMAs of this thread run in
+      // issue order, so the PV reads P before S_{j+2} overwrites it; the commit
+      // that tells the softmax S_{j+2} is done also covers that PV (O is stable
+      // when S_{j+2} is seen). The waits are blocking (bounded) waits.
+      auto issue_s = [&](int j) -> bool {
+        if (!warp_all(mbar_wait(k_full + j % SK, uint32_t(j / SK) & 1, st))) return false;
+        fence_proxy_async_smem();  // key rows landed by cp.async, read by the tensor core
+        tc_fence_after();
+        const uint32_t klo = desc_lo_kmajor(sbase + L::kK + (j % SK) * L::kTile);
+        const uint32_t tS = tmem + uint32_t((j & 1) * 128);
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            tc_mma_ss_lo_if(leader, tS, qlo + kstep_kmajor(ks), klo + kstep_kmajor(ks), kIdescQK, ks > 0 ? 1u : 0u);
-          tc_commit_if(leader, s_full + (ns & 1));
-          tc_commit_if(leader, k_empty + ns % SK);
-          issued = true;
-          ++ns;
-          did = true;
-        }
-        // P_np V_np: P written by warpgroup np%2 and the value rows in
-        if (np < ns && warp_all(mbar_test(p_full + (np & 1), uint32_t(np >> 1) & 1) &&
-                                mbar_test(v_full + np % SV, uint32_t(np / SV) & 1))) {
-          fence_proxy_async_smem();  // value rows landed by cp.async
-          tc_fence_after();
-          const uint32_t vlo = desc_lo_mnmajor(sbase + L::kV + (np % SV) * L::kTile);
-          const uint32_t tP = tmem + uint32_t((np & 1) * 128), tO = tmem + L::kColO + uint32_t((np & 1) * D);
+        for (int ks = 0; ks < D / 16; ++ks)
+          tc_mma_ss_lo_if(leader, tS, qlo + kstep_kmajor(ks), klo + kstep_kmajor(ks), kIdescQK, ks > 0 ? 1u : 0u);
+        tc_commit_if(leader, s_full + (j & 1));
+        tc_commit_if(leader, k_empty + j % SK);
+        issued = true;
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {
+        // P_j written by warpgroup j%2 and the value rows in
+        if (!warp_all(mbar_wait(p_full + (j & 1), uint32_t(j >> 1) & 1, st) &&
+                      mbar_wait(v_full + j % SV, uint32_t(j / SV) & 1, st)))
+          return false;
+        fence_proxy_async_smem();  // value rows landed by cp.async
+        tc_fence_after();
+        const uint32_t vlo = desc_lo_mnmajor(sbase + L::kV + (j % SV) * L::kTile);
+        const uint32_t tP = tmem + uint32_t((j & 1) * 128), tO = tmem + L::kColO + uint32_t((j & 1) * D);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            tc_mma_ts_lo_if(leader, tO, tP + ks * 8, vlo + kstep_mnmajor(ks), kIdescPV, (np >= 2 || ks > 0) ? 1u : 0u);
-          tc_commit_if(leader, v_empty + np % SV);
-          ++np;
-          did = true;
-        }
-        if (did) {
-          t0 = 0;
-        } else if ((it & 255u) == 0) {  // nothing could go: bounded wait
-          const uint64_t now = globaltimer_ns();
-          if (t0 == 0) t0 = now;
-          else if (now - t0 > kWaitLimitNs || (peek_status(st) & kStatusTimeout)) ok = false;
-          ok = warp_all(ok);
-        }
+        for (int ks = 0; ks < 8; ++ks)
+          tc_mma_ts_lo_if(leader, tO, tP + ks * 8, vlo + kstep_mnmajor(ks), kIdescPV, (j >= 2 || ks > 0) ? 1u : 0u);
+        tc_commit_if(leader, v_empty + j % SV);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok && T > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < T; ++j) {
+        ok = issue_pv(j);
+        if (ok && j + 2 < T) ok = issue_s(j + 2);
       }
       if (ok) tc_commit_if(leader, o_done);
       if (!ok) {
