@@ -2,9 +2,10 @@
 // two-pass paragraph: keep the K keys with the largest summed attention weight].
 // One CTA per row: an 8-bit-digit radix select finds the K-th largest score
 // (scores are non-negative fp32, so their bit patterns order like the values),
-// then an ordered block-scan compaction writes every key above it plus the
-// lowest-index keys equal to it, which gives ascending indices and the
-// ties-to-lower-index rule at once. The captured mass is summed in a fixed order.
+// then an ordered compaction (contiguous slice per warp, one scan over the
+// warps) writes every key above it plus the lowest-index keys equal to it,
+// which gives ascending indices and the ties-to-lower-index rule at once. The
+// captured mass is summed in a fixed order.
 #include "block_scan.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -14,26 +15,39 @@ namespace mcs {
 namespace {
 
 constexpr int kTopkThreads = 1024;
+constexpr int kTopkWarps = kTopkThreads / 32;
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) {
   __shared__ uint32_t hist[256];
-  __shared__ int warp_tot[32];
   __shared__ uint32_t sh_prefix, sh_remaining;
-  __shared__ float warp_sum[32];
+  __shared__ int wgt[kTopkWarps], weq[kTopkWarps];
+  __shared__ float warp_sum[kTopkWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x;
   const int grow = p.row0 + row;
   const float* S = p.scores + size_t(row) * p.N;
   const uint32_t* U = reinterpret_cast<const uint32_t*>(S);
+  const uint32_t lanes_below = (1u << lane) - 1u;
 
+  // Radix select, four 8-bit digits from the top. The block walks the row in
+  // chunks of 1024 so every warp stays converged; lanes of a warp that hit the
+  // same bin add their count with one shared-memory atomic (score exponents
+  // cluster, so a per-element atomic would serialise on a few bins).
   uint32_t prefix = 0, mask = 0, remaining = uint32_t(p.K);
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
     for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
-    for (int j = tid; j < p.N; j += kTopkThreads) {
-      const uint32_t u = U[j];
-      if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+    for (int c0 = 0; c0 < p.N; c0 += kTopkThreads) {
+      const int j = c0 + tid;
+      const uint32_t u = j < p.N ? U[j] : 0u;
+      const bool cand = j < p.N && (u & mask) == prefix;
+      const unsigned act = __ballot_sync(0xffffffffu, cand);
+      if (cand) {
+        const uint32_t bin = (u >> shift) & 255u;
+        const unsigned peers = __match_any_sync(act, bin);
+        if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], uint32_t(__popc(peers)));
+      }
     }
     __syncthreads();
     if (warp == 0) {
@@ -49,27 +63,59 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     remaining = sh_remaining;
     mask |= 0xFFu << shift;
   }
-  const uint32_t thr = prefix;       // bit pattern of the K-th largest score
-  const uint32_t need_eq = remaining; // how many scores equal to it are kept (lowest indices)
+  const uint32_t thr = prefix;                 // bit pattern of the K-th largest score
+  const int need_eq = int(remaining);          // how many scores equal to it are kept (lowest indices)
 
-  int32_t* out = p.idx + size_t(grow) * p.K;
-  int base_out = 0, base_eq = 0;
+  // Ordered compaction: warp w owns the contiguous slice [lo, hi) of the row.
+  // Counting pass, one exclusive scan over the warps' counts, then each warp
+  // writes its selected ids in index order with ballots (ties to the lower
+  // index: a warp keeps the first equal scores that the warps before it left).
+  const int span = ((p.N + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
+  const int lo = min(p.N, warp * span), hi = min(p.N, lo + span);
+  int cgt = 0, ceq = 0;
+  for (int j = lo + lane; j < hi; j += 32) {
+    const uint32_t u = U[j];
+    cgt += u > thr ? 1 : 0;
+    ceq += u == thr ? 1 : 0;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    cgt += __shfl_xor_sync(0xffffffffu, cgt, off);
+    ceq += __shfl_xor_sync(0xffffffffu, ceq, off);
+  }
+  if (lane == 0) {
+    wgt[warp] = cgt;
+    weq[warp] = ceq;
+  }
+  __syncthreads();
+  int gt_before = 0, eq_before = 0, gt_all = 0, eq_all = 0;
+  for (int w = 0; w < kTopkWarps; ++w) {
+    const int a = wgt[w], b = weq[w];
+    gt_before += w < warp ? a : 0;
+    eq_before += w < warp ? b : 0;
+    gt_all += a;
+    eq_all += b;
+  }
+  const int take_eq = max(0, min(ceq, need_eq - eq_before));
+  int out_pos = gt_before + min(eq_before, need_eq);
+  int eq_seen = 0;
   float msum = 0.f;
-  for (int c0 = 0; c0 < p.N; c0 += kTopkThreads) {
-    const int j = c0 + tid;
-    const bool valid = j < p.N;
-    const uint32_t u = valid ? U[j] : 0u;
-    const bool gt = valid && u > thr, eq = valid && u == thr;
-    int eq_tot, sel_tot;
-    const int eq_pre = block_excl_count(eq, warp_tot, &eq_tot);
-    const bool sel = gt || (eq && uint32_t(base_eq + eq_pre) < need_eq);
-    const int sel_pre = block_excl_count(sel, warp_tot, &sel_tot);
-    if (sel && base_out + sel_pre < p.K) {
-      out[base_out + sel_pre] = j;
+  int32_t* out = p.idx + size_t(grow) * p.K;
+  for (int c = lo; c < hi; c += 32) {
+    const int j = c + lane;
+    const bool v = j < hi;
+    const uint32_t u = v ? U[j] : 0u;
+    const bool gt = v && u > thr, eq = v && u == thr;
+    const unsigned beq = __ballot_sync(0xffffffffu, eq);
+    const bool sel = gt || (eq && eq_seen + __popc(beq & lanes_below) < take_eq);
+    const unsigned bsel = __ballot_sync(0xffffffffu, sel);
+    const int pos = out_pos + __popc(bsel & lanes_below);
+    if (sel && pos < p.K) {
+      out[pos] = j;
       msum += __uint_as_float(u);
     }
-    base_eq += eq_tot;
-    base_out += sel_tot;
+    out_pos += __popc(bsel);
+    eq_seen += __popc(beq);
   }
   if (p.mass != nullptr) {
     const int bh = grow / p.G, g = grow % p.G;
@@ -85,11 +131,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     __syncthreads();
     if (tid == 0) {
       float tsum = 0.f;
-      for (int w = 0; w < kTopkThreads / 32; ++w) tsum += warp_sum[w];
+      for (int w = 0; w < kTopkWarps; ++w) tsum += warp_sum[w];
       p.mass[grow] = nreal > 0 ? tsum / float(nreal) : 0.f;
     }
   }
-  if (tid == 0 && base_out != p.K) raise_status(p.status, kStatusBounds);
+  if (tid == 0 && gt_all + min(eq_all, need_eq) != p.K) raise_status(p.status, kStatusBounds);
 }
 
 }  // namespace
