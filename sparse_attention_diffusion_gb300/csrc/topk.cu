@@ -38,15 +38,25 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     const int shift = 24 - 8 * pass;
     for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
-    for (int c0 = 0; c0 < p.N; c0 += kTopkThreads) {
-      const int j = c0 + tid;
-      const uint32_t u = j < p.N ? U[j] : 0u;
-      const bool cand = j < p.N && (u & mask) == prefix;
-      const unsigned act = __ballot_sync(0xffffffffu, cand);
-      if (cand) {
-        const uint32_t bin = (u >> shift) & 255u;
-        const unsigned peers = __match_any_sync(act, bin);
-        if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], uint32_t(__popc(peers)));
+    // four chunks per step: their loads are issued together (the row does not
+    // fit in L1, so each is an L2 round trip)
+    for (int c0 = 0; c0 < p.N; c0 += 4 * kTopkThreads) {
+      uint32_t u4[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int j = c0 + k * kTopkThreads + tid;
+        u4[k] = j < p.N ? __ldg(U + j) : 0u;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int j = c0 + k * kTopkThreads + tid;
+        const bool cand = j < p.N && (u4[k] & mask) == prefix;
+        const unsigned act = __ballot_sync(0xffffffffu, cand);
+        if (cand) {
+          const uint32_t bin = (u4[k] >> shift) & 255u;
+          const unsigned peers = __match_any_sync(act, bin);
+          if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], uint32_t(__popc(peers)));
+        }
       }
     }
     __syncthreads();
@@ -73,10 +83,19 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   const int span = ((p.N + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
   const int lo = min(p.N, warp * span), hi = min(p.N, lo + span);
   int cgt = 0, ceq = 0;
-  for (int j = lo + lane; j < hi; j += 32) {
-    const uint32_t u = U[j];
-    cgt += u > thr ? 1 : 0;
-    ceq += u == thr ? 1 : 0;
+  for (int c = lo; c < hi; c += 128) {
+    uint32_t u4[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int j = c + k * 32 + lane;
+      u4[k] = j < hi ? __ldg(U + j) : 0u;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const bool v = c + k * 32 + lane < hi;
+      cgt += (v && u4[k] > thr) ? 1 : 0;
+      ceq += (v && u4[k] == thr) ? 1 : 0;
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -101,21 +120,29 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   int eq_seen = 0;
   float msum = 0.f;
   int32_t* out = p.idx + size_t(grow) * p.K;
-  for (int c = lo; c < hi; c += 32) {
-    const int j = c + lane;
-    const bool v = j < hi;
-    const uint32_t u = v ? U[j] : 0u;
-    const bool gt = v && u > thr, eq = v && u == thr;
-    const unsigned beq = __ballot_sync(0xffffffffu, eq);
-    const bool sel = gt || (eq && eq_seen + __popc(beq & lanes_below) < take_eq);
-    const unsigned bsel = __ballot_sync(0xffffffffu, sel);
-    const int pos = out_pos + __popc(bsel & lanes_below);
-    if (sel && pos < p.K) {
-      out[pos] = j;
-      msum += __uint_as_float(u);
+  for (int c = lo; c < hi; c += 128) {
+    uint32_t u4[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int j = c + k * 32 + lane;
+      u4[k] = j < hi ? __ldg(U + j) : 0u;
     }
-    out_pos += __popc(bsel);
-    eq_seen += __popc(beq);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {  // chunks in index order
+      const int j = c + k * 32 + lane;
+      const bool v = j < hi;
+      const bool gt = v && u4[k] > thr, eq = v && u4[k] == thr;
+      const unsigned beq = __ballot_sync(0xffffffffu, eq);
+      const bool sel = gt || (eq && eq_seen + __popc(beq & lanes_below) < take_eq);
+      const unsigned bsel = __ballot_sync(0xffffffffu, sel);
+      const int pos = out_pos + __popc(bsel & lanes_below);
+      if (sel && pos < p.K) {
+        out[pos] = j;
+        msum += __uint_as_float(u4[k]);
+      }
+      out_pos += __popc(bsel);
+      eq_seen += __popc(beq);
+    }
   }
   if (p.mass != nullptr) {
     const int bh = grow / p.G, g = grow % p.G;
