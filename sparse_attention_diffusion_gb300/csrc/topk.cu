@@ -16,6 +16,7 @@ namespace {
 
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kLoads = 8;  // independent row loads in flight per thread
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) {
   __shared__ uint32_t hist[256];
@@ -38,17 +39,17 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     const int shift = 24 - 8 * pass;
     for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
-    // four chunks per step: their loads are issued together (the row does not
+    // kLoads chunks per step: their loads are issued together (the row does not
     // fit in L1, so each is an L2 round trip)
-    for (int c0 = 0; c0 < p.N; c0 += 4 * kTopkThreads) {
-      uint32_t u4[4];
+    for (int c0 = 0; c0 < p.N; c0 += kLoads * kTopkThreads) {
+      uint32_t u4[kLoads];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < kLoads; ++k) {
         const int j = c0 + k * kTopkThreads + tid;
         u4[k] = j < p.N ? __ldg(U + j) : 0u;
       }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < kLoads; ++k) {
         const int j = c0 + k * kTopkThreads + tid;
         const bool cand = j < p.N && (u4[k] & mask) == prefix;
         const unsigned act = __ballot_sync(0xffffffffu, cand);
@@ -83,15 +84,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   const int span = ((p.N + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
   const int lo = min(p.N, warp * span), hi = min(p.N, lo + span);
   int cgt = 0, ceq = 0;
-  for (int c = lo; c < hi; c += 128) {
-    uint32_t u4[4];
+  for (int c = lo; c < hi; c += kLoads * 32) {
+    uint32_t u4[kLoads];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kLoads; ++k) {
       const int j = c + k * 32 + lane;
       u4[k] = j < hi ? __ldg(U + j) : 0u;
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kLoads; ++k) {
       const bool v = c + k * 32 + lane < hi;
       cgt += (v && u4[k] > thr) ? 1 : 0;
       ceq += (v && u4[k] == thr) ? 1 : 0;
@@ -120,15 +121,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   int eq_seen = 0;
   float msum = 0.f;
   int32_t* out = p.idx + size_t(grow) * p.K;
-  for (int c = lo; c < hi; c += 128) {
-    uint32_t u4[4];
+  for (int c = lo; c < hi; c += kLoads * 32) {
+    uint32_t u4[kLoads];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kLoads; ++k) {
       const int j = c + k * 32 + lane;
       u4[k] = j < hi ? __ldg(U + j) : 0u;
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {  // chunks in index order
+    for (int k = 0; k < kLoads; ++k) {  // chunks in index order
       const int j = c + k * 32 + lane;
       const bool v = j < hi;
       const bool gt = v && u4[k] > thr, eq = v && u4[k] == thr;
