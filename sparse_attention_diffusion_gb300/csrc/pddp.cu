@@ -148,40 +148,60 @@ __device__ __forceinline__ float ld_f(const T* p) {
   return to_f32(*p);
 }
 
-// 1. per-chunk sums of real members
+// 1. per-chunk sums of real members: thread (row lane rl, chunk cc) sums the
+// 16-byte chunk cc of rows rl, rl + RL, ..., four rows in flight at a time; the
+// row lanes are then added in a fixed order
 template <typename T, typename A, int D>
 __global__ void __launch_bounds__(256) sum_kernel(const T* __restrict__ x, const int32_t* __restrict__ perm, Tables t,
                                                   int level, int N, int N_pad, int C, int G, A* psum, int* pcnt,
                                                   int max_chunks) {
-  constexpr int kLanes = 256 / D;
-  __shared__ A part[256];
-  __shared__ int cnt_part[kLanes];
+  constexpr int V = 16 / int(sizeof(T));  // elements per 16-byte chunk
+  constexpr int CPR = D / V;              // chunks per row
+  constexpr int RL = 256 / CPR;           // row lanes
+  constexpr int R = 4;
+  __shared__ A part[RL][D];
+  __shared__ int cnt_part[RL];
   const int c = blockIdx.x, bh = blockIdx.y;
   const size_t to = size_t(level) * G + c;
   const int g0 = t.chunk_g0[to], ng = t.chunk_ng[to];
-  const int dim = threadIdx.x % D, rl = threadIdx.x / D;
+  const int cc = threadIdx.x % CPR, rl = threadIdx.x / CPR;
   const int32_t* pr = perm + size_t(bh) * N_pad + size_t(g0) * C;
-  const T* xb = x + size_t(bh) * N * D;
-  A acc = 0;
+  const T* xb = x + size_t(bh) * N * D + cc * V;
+  A acc[V];
+#pragma unroll
+  for (int k = 0; k < V; ++k) acc[k] = 0;
   int cnt = 0;
-  for (int r = rl; r < ng * C; r += kLanes) {
-    const int tok = pr[r];
-    if (tok < N) {
-      acc += A(to_f32(xb[size_t(tok) * D + dim]));
-      ++cnt;
+  const int rows = ng * C;
+  for (int r0 = rl; r0 < rows; r0 += R * RL) {
+    int tok[R];
+#pragma unroll
+    for (int q = 0; q < R; ++q) tok[q] = r0 + q * RL < rows ? pr[r0 + q * RL] : N;
+    uint4 raw[R];
+#pragma unroll
+    for (int q = 0; q < R; ++q)
+      if (tok[q] < N) raw[q] = *reinterpret_cast<const uint4*>(xb + size_t(tok[q]) * D);
+#pragma unroll
+    for (int q = 0; q < R; ++q) {
+      if (tok[q] < N) {
+        const T* vals = reinterpret_cast<const T*>(&raw[q]);
+#pragma unroll
+        for (int k = 0; k < V; ++k) acc[k] += A(to_f32(vals[k]));
+        ++cnt;
+      }
     }
   }
-  part[threadIdx.x] = acc;
-  if (dim == 0) cnt_part[rl] = cnt;
+#pragma unroll
+  for (int k = 0; k < V; ++k) part[rl][cc * V + k] = acc[k];
+  if (cc == 0) cnt_part[rl] = cnt;
   __syncthreads();
   if (threadIdx.x < D) {
     A s = 0;
-    for (int l = 0; l < kLanes; ++l) s += part[l * D + threadIdx.x];
+    for (int l = 0; l < RL; ++l) s += part[l][threadIdx.x];
     psum[(size_t(bh) * max_chunks + c) * D + threadIdx.x] = s;
   }
   if (threadIdx.x == 0) {
     int s = 0;
-    for (int l = 0; l < kLanes; ++l) s += cnt_part[l];
+    for (int l = 0; l < RL; ++l) s += cnt_part[l];
     pcnt[size_t(bh) * max_chunks + c] = s;
   }
 }
@@ -227,16 +247,25 @@ __global__ void __launch_bounds__(256) cov_kernel(const T* __restrict__ x, const
   const T* xb = x + size_t(bh) * N * D;
   const int rows = ng * C;
   __syncthreads();
+  // rows are staged 16 bytes at a time (one index lookup per 16-byte chunk of a
+  // row), then centred; the products below are the same in the same order
+  constexpr int V = 16 / int(sizeof(T));  // elements per 16-byte chunk
+  constexpr int CPR = D / V;              // chunks per row
   for (int r0 = 0; r0 < rows; r0 += RB) {
-    for (int e = threadIdx.x; e < RB * D; e += 256) {
-      const int rr = e / D, dd = e % D;
+    for (int e = threadIdx.x; e < RB * CPR; e += 256) {
+      const int rr = e / CPR, cc = e % CPR;
       const int r = r0 + rr;
-      A val = 0;
-      if (r < rows) {
-        const int tok = pr[r];
-        if (tok < N) val = A(to_f32(xb[size_t(tok) * D + dd])) - mu[dd];
+      int tok = N;
+      if (r < rows) tok = pr[r];
+      if (tok < N) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(xb + size_t(tok) * D + cc * V);
+        const T* vals = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+        for (int k = 0; k < V; ++k) xs[rr][cc * V + k] = A(to_f32(vals[k])) - mu[cc * V + k];
+      } else {
+#pragma unroll
+        for (int k = 0; k < V; ++k) xs[rr][cc * V + k] = A(0);
       }
-      xs[rr][dd] = val;
     }
     __syncthreads();
 #pragma unroll 4
@@ -310,7 +339,7 @@ __device__ __forceinline__ uint64_t order_key(double f) {
   return (u >> 63) ? ~u : (u | (uint64_t(1) << 63));
 }
 
-// 4. projection keys, one warp per member
+// 4. projection keys, one warp per member (four members per warp iteration)
 template <typename T, typename A, int D, typename KeyT>
 __global__ void __launch_bounds__(256) keys_kernel(const T* __restrict__ x, const int32_t* __restrict__ perm, Tables t,
                                                    int level, int N, int N_pad, int C, int G, const A* node_mu,
@@ -327,15 +356,40 @@ __global__ void __launch_bounds__(256) keys_kernel(const T* __restrict__ x, cons
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const size_t base = size_t(bh) * N_pad + size_t(g0) * C;
   const T* xb = x + size_t(bh) * N * D;
-  for (int r = warp; r < ng * C; r += 8) {
-    const int tok = perm[base + r];
-    A s = 0;
-    if (tok < N) {
-      for (int dd = lane; dd < D; dd += 32) s += (A(to_f32(xb[size_t(tok) * D + dd])) - mu[dd]) * vv[dd];
+  // lane l holds elements [l*E, l*E + E) of a row (one vector load); four rows
+  // per warp iteration so their loads are in flight together
+  constexpr int E = D / 32;
+  constexpr int R = 4;
+  const int rows = ng * C;
+  for (int r0 = warp * R; r0 < rows; r0 += 8 * R) {
+    int tok[R];
+#pragma unroll
+    for (int q = 0; q < R; ++q) tok[q] = r0 + q < rows ? perm[base + r0 + q] : N;
+    A vals[R][E];
+#pragma unroll
+    for (int q = 0; q < R; ++q) {
+      T raw[E];
+      if (tok[q] < N) {
+        const T* src = xb + size_t(tok[q]) * D + lane * E;
+        if constexpr (E * sizeof(T) == 16) *reinterpret_cast<uint4*>(raw) = *reinterpret_cast<const uint4*>(src);
+        else if constexpr (E * sizeof(T) == 8) *reinterpret_cast<uint2*>(raw) = *reinterpret_cast<const uint2*>(src);
+        else *reinterpret_cast<uint32_t*>(raw) = *reinterpret_cast<const uint32_t*>(src);
+      } else {
+#pragma unroll
+        for (int k = 0; k < E; ++k) raw[k] = from_f32<T>(0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < E; ++k) vals[q][k] = A(to_f32(raw[k]));
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) keys[base + r] = tok < N ? order_key(s) : ~KeyT(0);
+    for (int q = 0; q < R; ++q) {
+      A s = 0;
+#pragma unroll
+      for (int k = 0; k < E; ++k) s += (vals[q][k] - mu[lane * E + k]) * vv[lane * E + k];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      if (lane == 0 && r0 + q < rows) keys[base + r0 + q] = tok[q] < N ? order_key(s) : ~KeyT(0);
+    }
   }
 }
 
