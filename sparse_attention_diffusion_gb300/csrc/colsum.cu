@@ -4,15 +4,17 @@
 // with lse from pass 1 (the dense kernel) [MC-Sparse summary: anchor two-pass
 // paragraph: the extra QK pass recomputes the probabilities].
 //
-// One CTA per group, 192 threads:
-//   warps 0-3   gather the group's query rows (through perm) once, then per key
-//               tile read the transposed logits S^T = K_tile Q_g^T from tensor
+// One CTA per group, 320 threads:
+//   warps 0-7   two warpgroups taking alternate key tiles: warps 0-3 first gather
+//               the group's query rows (through perm); per key tile a warpgroup
+//               reads the transposed logits S^T = K_tile Q_g^T from tensor
 //               memory: the TMEM lane is the key, so each thread sums its key's
 //               exp over the group's queries with no cross-thread reduction, and
 //               writes the key's score (consecutive threads, consecutive keys);
-//   warp 4      tensor-memory allocation and the single MMA-issuing thread; four
+//               two warps per sub-partition hide each other's load latency;
+//   warp 8      tensor-memory allocation and the single MMA-issuing thread; four
 //               (C = 128) or eight (C = 64) S^T buffers let it run ahead;
-//   warp 5      TMA producer: key tiles of 128 rows as tiled boxes of a 3-D
+//   warp 9      TMA producer: key tiles of 128 rows as tiled boxes of a 3-D
 //               tensor map into a 6-stage (d = 128) ring; rows >= N read zeros.
 // All waits are bounded; on a timeout the CTA flags it, lets its copies and
 // MMAs land, frees tensor memory and returns.
@@ -25,7 +27,8 @@
 namespace mcs {
 namespace {
 
-constexpr int kColThreads = 192;
+constexpr int kColThreads = 320;
+constexpr int kColMmaWarp = 8, kColTmaWarp = 9;
 
 template <int D, int CQ>
 struct ColCfg {
@@ -79,7 +82,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
     mbar_init(drain, 1);
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == kColMmaWarp) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -88,10 +91,10 @@ __global__ void __launch_bounds__(kColThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 4) {
+  if (warp < 8) {
     // ------------------------------------------------------------ query rows, then column sums
     const int32_t* permg = p.perm + size_t(bh) * p.N_pad + size_t(g) * p.C;
-    {
+    if (warp < 4) {
       constexpr int kChunks = D / 8, kRowsPerPass = 128 / kChunks;
       const int ch = tid % kChunks, r0 = tid / kChunks;
       const __nv_bfloat16* qb = p.q + size_t(bh) * p.N * D;
@@ -118,14 +121,16 @@ __global__ void __launch_bounds__(kColThreads, 1)
       cp_async_wait<0>();
       fence_proxy_async_smem();
       mbar_arrive(q_full);
-      named_bar_sync(2, 128);  // nlse visible to all column threads
     }
-    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    named_bar_sync(2, 256);  // nlse visible to all column threads
+    // two warpgroups take alternate key tiles (tile j uses S^T buffer j % NB)
+    const int wg = warp >> 2;
+    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     float* out = p.scores + size_t(blockIdx.x) * p.N;
     const float sl2 = p.scale_log2;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
     bool ok = true;
-    for (int j = 0; j < T; ++j) {
+    for (int j = wg; j < T; j += 2) {
       const int b = j % NB;
       if (!warp_all(mbar_wait(s_full + b, uint32_t(j / NB) & 1, st))) {
         ok = false;
@@ -150,13 +155,13 @@ __global__ void __launch_bounds__(kColThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(s_free + b);
-      const int key = j * 128 + tid;
+      const int key = j * 128 + (tid & 127);
       float a0, a1;
       f2_unpack(f2_add(acc2[0], acc2[1]), a0, a1);
       if (key < p.N) out[key] = a0 + a1;
     }
     if (!ok && tid == 0) raise_status(st, kStatusTimeout);
-  } else if (warp == 5) {
+  } else if (warp == kColTmaWarp) {
     // ------------------------------------------------------------ TMA producer
     int armed = 0;
     if (lane == 0) {
@@ -178,7 +183,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
       for (int t = (armed > S ? armed - S : 0); t < armed; ++t) mbar_wait(k_full + t % S, (t / S) & 1, st);
     }
     __syncwarp();
-  } else if (warp == 4) {
+  } else if (warp == kColMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdesc = idesc_bf16_f32(128, CQ, 0, 0);
@@ -208,7 +213,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == kColMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
