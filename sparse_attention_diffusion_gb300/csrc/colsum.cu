@@ -137,24 +137,30 @@ __global__ void __launch_bounds__(kColThreads, 1)
         break;
       }
       tc_fence_after();
-      // packed pairs: one FMA for two logits, two packed partial sums (four lanes)
-      uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-#pragma unroll
-      for (int c0 = 0; c0 < CQ; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + b * CQ + c0, r);
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 nl = *reinterpret_cast<const float4*>(nlse + c0 + i);
-          float x0, x1, x2, x3;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), sl2x2, f2_pack(nl.x, nl.y)), x0, x1);
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])), sl2x2, f2_pack(nl.z, nl.w)), x2, x3);
-          acc2[0] = f2_add(acc2[0], f2_pack(ex2_approx(x0), ex2_approx(x1)));
-          acc2[1] = f2_add(acc2[1], f2_pack(ex2_approx(x2), ex2_approx(x3)));
-        }
+      // the key's whole S^T row in one load (one wait), then the buffer goes
+      // back to the MMA thread before the exponentials
+      uint32_t r[CQ];
+      if constexpr (CQ == 128) {
+        tmem_ld128(tmem + lane_off + b * CQ, r);
+      } else {
+        uint32_t (&r0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
+        uint32_t (&r1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
+        tmem_ld32(tmem + lane_off + b * CQ, r0);
+        tmem_ld32(tmem + lane_off + b * CQ + 32, r1);
       }
       tc_fence_before();
       mbar_arrive(s_free + b);
+      // packed pairs: one FMA for two logits, two packed partial sums (four lanes)
+      uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+      for (int i = 0; i < CQ; i += 4) {
+        const float4 nl = *reinterpret_cast<const float4*>(nlse + i);
+        float x0, x1, x2, x3;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), sl2x2, f2_pack(nl.x, nl.y)), x0, x1);
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])), sl2x2, f2_pack(nl.z, nl.w)), x2, x3);
+        acc2[0] = f2_add(acc2[0], f2_pack(ex2_approx(x0), ex2_approx(x1)));
+        acc2[1] = f2_add(acc2[1], f2_pack(ex2_approx(x2), ex2_approx(x3)));
+      }
       const int key = j * 128 + (tid & 127);
       float a0, a1;
       f2_unpack(f2_add(acc2[0], acc2[1]), a0, a1);
