@@ -1,0 +1,93 @@
+"""The 720p kernel-benchmark layer at full size, in the launch configuration the
+benchmark times (B=1, H=40, N=75,600 on a 21x45x80 grid, d=128, bf16, C=128,
+K=15,120): the whole path runs on the GPU (grouping, dense attention + LSE,
+pass-2 selection, anchor residual, one drifted reuse step), and sampled heads,
+groups and rows are checked one by one against the float64 oracle fed the very
+tensors the GPU received (the oracle cannot run the whole layer in a test)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import mcs_oracle as orc
+from sparse_attention_diffusion_gb300 import mcs, synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+HEADS = (0, 17, 39)        # sampled heads
+GROUPS_PER_HEAD = 2        # sampled groups per head (selection, residual, reuse)
+ROWS_PER_HEAD = 64         # sampled query rows per head (dense output and LSE)
+
+
+@pytest.fixture(scope="module")
+def run():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    mcs.load(build_if_missing=True)
+    wl = synth.KBENCH_720P
+    layer = synth.make_layer(wl, device="cuda")
+    q, k, v = layer.cast()
+    desc = mcs.desc_for(q, wl.C)
+    K = wl.K
+    cache = mcs.alloc_cache(desc, K, q.dtype)
+    ws = mcs.workspace(desc, K)
+    o_dense = torch.empty_like(q)
+    lse = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32, device="cuda")
+    mcs.mcs_group_pddp(desc, q, cache["perm"], cache["group_of"], ws)
+    mcs.mcs_dense_attn(desc, q, k, v, o_dense, lse)
+    mcs.mcs_anchor_select(desc, q, k, cache["perm"], lse, K, cache["idx"], cache["mass"], ws)
+    mcs.mcs_anchor_residual(desc, q, k, v, cache["perm"], cache["idx"], K, o_dense, cache["residual"])
+    layer.drift_step()
+    q2, k2, v2 = layer.cast()
+    o_reuse = torch.empty_like(q2)
+    mcs.mcs_sparse_attn_gather(desc, q2, k2, v2, cache["perm"], cache["idx"], K, cache["residual"], o_reuse)
+    mcs.mcs_check_status()
+    torch.cuda.synchronize()
+    host = lambda t, h: parity.f64(t[0, h])
+    out = dict(wl=wl, K=K, heads={})
+    rng = np.random.default_rng(20261202)
+    for h in HEADS:
+        out["heads"][h] = dict(
+            q=host(q, h), k=host(k, h), v=host(v, h), q2=host(q2, h), k2=host(k2, h), v2=host(v2, h),
+            o_dense=host(o_dense, h), lse=lse[0, h].double().cpu().numpy(), o_reuse=host(o_reuse, h),
+            residual=host(cache["residual"], h), perm=cache["perm"][0, h].cpu().numpy(),
+            group_of=cache["group_of"][0, h].cpu().numpy(), idx=cache["idx"][0, h].cpu().numpy(),
+            mass=cache["mass"][0, h].cpu().numpy(),
+            rows=rng.choice(wl.N, ROWS_PER_HEAD, replace=False),
+            groups=rng.choice(wl.G, GROUPS_PER_HEAD, replace=False))
+    return out
+
+
+def test_groups_fullsize(run):
+    wl = run["wl"]
+    for h, d in run["heads"].items():
+        parity.assert_valid_partition(d["perm"], wl.N, wl.C)
+        gid = np.empty(wl.N, dtype=np.int64)
+        for g in range(wl.G):
+            gid[parity.group_members(d["perm"], g, wl.C, wl.N)] = g
+        assert np.array_equal(d["group_of"], gid), f"head {h}: group_of disagrees with perm"
+
+
+def test_dense_rows_fullsize(run):
+    for h, d in run["heads"].items():
+        rows = d["rows"]
+        o_ref, lse_ref = orc.dense_attention(d["q"][rows], d["k"], d["v"])
+        parity.assert_close(d["o_dense"][rows], o_ref, "bf16", f"dense rows head {h}")
+        assert np.abs(d["lse"][rows] - lse_ref).max() < 1e-3, f"head {h}: lse"
+
+
+def test_selection_residual_reuse_fullsize(run):
+    wl, K = run["wl"], run["K"]
+    for h, d in run["heads"].items():
+        for g in d["groups"]:
+            mem = parity.group_members(d["perm"], g, wl.C, wl.N)
+            # pass 2 on this group with the oracle's own pass-1 lse of its queries
+            _, lse_g = orc.dense_attention(d["q"][mem], d["k"], np.zeros((wl.N, 1)))
+            S = orc.group_scores(d["q"][mem], lse_g, d["k"])
+            parity.check_selection(d["idx"][g], S, K, mem.size, f"head {h} group {g}")
+            assert abs(d["mass"][g] - orc.captured_mass(S, d["idx"][g], mem.size)) < 1e-4
+            # residual of the anchor step (the GPU's own dense output, as the path uses it)
+            r_ref = d["o_dense"][mem] - orc.sparse_attention(d["q"][mem], d["k"], d["v"], d["idx"][g])
+            parity.assert_close(d["residual"][mem], r_ref, "bf16", f"residual head {h} group {g}")
+            # reuse step on the drifted inputs over the cached group, indices and residual
+            want = orc.sparse_attention(d["q2"][mem], d["k2"], d["v2"], d["idx"][g]) + d["residual"][mem]
+            parity.assert_close(d["o_reuse"][mem], want, "bf16", f"reuse head {h} group {g}")
