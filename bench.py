@@ -14,7 +14,9 @@ reuse kernel; the roofline object covers that kernel (kept FLOPs / time against
 the measured sustained bf16 peak). After the timed steps (outside the timed
 region) the 118,800-token schedule (24 heads, 50 steps, densities 0.15 and 0.25)
 runs once to report the total time including anchors and the anchor overhead as
-equivalent extra density (`anchor_overhead`; `--no-schedule` skips it).
+equivalent extra density (`anchor_overhead`; `--no-schedule` skips it), and the
+65,536-token density/tile sweep (d and C in {64, 128}, densities 0.05-1.0) reports
+the sparse kernel against the dense kernel per point (`sweep`; `--no-sweep`).
 `--impl reference` times the float64 CPU oracle instead, on a bounded sample of
 groups, extrapolated to ms/layer.
 """
@@ -52,6 +54,7 @@ def parse():
     ap.add_argument("--density", default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-schedule", action="store_true", help="skip the 118,800-token schedule (anchor overhead)")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the 65,536-token density/tile sweep")
     ap.add_argument("--heads", type=int, default=None, help="override H (smaller case for profiler captures)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget (CPU seconds)")
     return ap.parse_args()
@@ -220,6 +223,59 @@ def schedule_overhead(dev):
     return out
 
 
+def sweep_table(dev, peak_tflops):
+    """The density/tile sweep layer (16 heads, N = 65,536, bf16) for d and C in
+    {64, 128}: groups and dense attention once per (d, C), then for every density
+    the anchor selection and the reuse-step sparse kernel, timed with CUDA events
+    (median of 5 launches) against the dense kernel (median of 3)."""
+    import torch
+
+    from sparse_attention_diffusion_gb300 import mcs, synth
+
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, n):
+        ts = []
+        for _ in range(n):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    rows = []
+    for d, C in ((128, 128), (128, 64), (64, 128), (64, 64)):
+        wl0 = synth.SWEEP.with_(d=d, C=C)
+        layer = synth.make_layer(wl0, device=dev)
+        q, k, v = layer.cast()
+        del layer
+        desc = mcs.desc_for(q, C)
+        o_dense = torch.empty_like(q)
+        lse = torch.empty((wl0.B, wl0.H, wl0.N), dtype=torch.float32, device=dev)
+        o = torch.empty_like(q)
+        cache = mcs.alloc_cache(desc, wl0.N, q.dtype, device=dev)
+        ws = mcs.workspace(desc, wl0.N, device=dev)
+        mcs.mcs_group_pddp(desc, q, cache["perm"], cache["group_of"], ws)
+        t_dense = timed(lambda: mcs.mcs_dense_attn(desc, q, k, v, o_dense, lse), 3)
+        for rho in ("0.05", "0.1", "0.15", "0.2", "0.3", "0.5", "1.0"):
+            K = synth.SWEEP.with_(d=d, C=C, density=rho).K
+            idx = cache["idx"].view(-1)[: wl0.B * wl0.H * wl0.G * K].view(wl0.B, wl0.H, wl0.G, K)
+            mcs.mcs_anchor_select(desc, q, k, cache["perm"], lse, K, idx, cache["mass"], ws)
+            mcs.mcs_anchor_residual(desc, q, k, v, cache["perm"], idx, K, o_dense, cache["residual"])
+            t = timed(lambda: mcs.mcs_sparse_attn_gather(desc, q, k, v, cache["perm"], idx, K, cache["residual"], o), 5)
+            tf = 4.0 * wl0.B * wl0.H * wl0.N * K * d / (t * 1e-3) / 1e12
+            rows.append({"d": d, "C": C, "density": float(rho), "K": K, "sparse_ms": t, "tflops": tf,
+                         "frac": tf / peak_tflops, "dense_ms": t_dense, "speedup_vs_dense": t_dense / t,
+                         "ideal_speedup": 1.0 / float(rho)})
+        mcs.mcs_check_status()
+        del q, k, v, o_dense, lse, o, cache, ws
+        torch.cuda.empty_cache()
+    return {"workload": synth.SWEEP.name, "B": 1, "H": synth.SWEEP.H, "N": synth.SWEEP.N,
+            "peak_kind": "measured sustained bf16", "rows": rows}
+
+
 def run_mcs(args, wl, K):
     import torch
     import torch.distributed as dist
@@ -363,6 +419,8 @@ def run_mcs(args, wl, K):
         }
         if world == 1 and not args.no_schedule:
             line["anchor_overhead"] = schedule_overhead(dev)
+        if world == 1 and not args.no_sweep:
+            line["sweep"] = sweep_table(dev, pk["bf16_sus"])
         if world == 1 and not args.no_cpu_baseline:
             dt, g, thr = oracle_sample(wl, K, args.cpu_seconds)
             val = dt / g * wl.B * wl.H * wl.G * 1e3

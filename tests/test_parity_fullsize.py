@@ -91,3 +91,36 @@ def test_selection_residual_reuse_fullsize(run):
             # reuse step on the drifted inputs over the cached group, indices and residual
             want = orc.sparse_attention(d["q2"][mem], d["k2"], d["v2"], d["idx"][g]) + d["residual"][mem]
             parity.assert_close(d["o_reuse"][mem], want, "bf16", f"reuse head {h} group {g}")
+
+
+@pytest.mark.parametrize("d,C", [(128, 128), (64, 64)])
+def test_sweep_layer_k_equals_n(d, C):
+    """The 65,536-token sweep layer at density 1.0 (K = N): the anchor's sparse
+    output reproduces dense attention, so the residual is zero, and a reuse step
+    on the unchanged inputs reproduces the dense output [residual paragraph]."""
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    mcs.load(build_if_missing=True)
+    wl = synth.SWEEP.with_(d=d, C=C, density="1.0")
+    layer = synth.make_layer(wl, device="cuda")
+    q, k, v = layer.cast()
+    desc = mcs.desc_for(q, wl.C)
+    K = wl.K
+    assert K == wl.N
+    cache = mcs.alloc_cache(desc, K, q.dtype)
+    ws = mcs.workspace(desc, K)
+    o_dense = torch.empty_like(q)
+    lse = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32, device="cuda")
+    mcs.mcs_group_pddp(desc, q, cache["perm"], cache["group_of"], ws)
+    mcs.mcs_dense_attn(desc, q, k, v, o_dense, lse)
+    mcs.mcs_anchor_select(desc, q, k, cache["perm"], lse, K, cache["idx"], cache["mass"], ws)
+    mcs.mcs_anchor_residual(desc, q, k, v, cache["perm"], cache["idx"], K, o_dense, cache["residual"])
+    o_reuse = torch.empty_like(q)
+    mcs.mcs_sparse_attn_gather(desc, q, k, v, cache["perm"], cache["idx"], K, cache["residual"], o_reuse)
+    mcs.mcs_check_status()
+    want_idx = torch.arange(wl.N, dtype=torch.int32, device="cuda")
+    assert torch.equal(cache["idx"], want_idx.expand_as(cache["idx"])), "K = N must select every key"
+    assert torch.allclose(cache["mass"], torch.ones_like(cache["mass"]), atol=1e-4), "K = N keeps all the mass"
+    R = cache["residual"].float()
+    err = (o_reuse.float() - o_dense.float()).abs()
+    assert float(R.abs().max()) <= 2e-2 and float(R.pow(2).mean().sqrt()) <= 5e-3, "residual not ~0"
+    assert float(err.max()) <= 2e-2 and float(err.pow(2).mean().sqrt()) <= 5e-3, "reuse != dense"
