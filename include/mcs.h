@@ -136,6 +136,28 @@ mcs_status mcs_sparse_attn_gather(const mcs_desc *desc, const void *q, const voi
                                   const int32_t *perm, const int32_t *idx, int K,
                                   const void *residual, void *o, mcs_stream stream);
 
+/* Host-to-host form of mcs_sparse_attn_gather for a reuse step whose current
+ * q, k, v live in host memory and whose output is wanted there (the method has
+ * no counterpart: this is a deployment variant). Same computation and result as
+ * mcs_sparse_attn_gather, bit for bit. q_host, k_host, v_host: [B,H,N,d] host
+ * buffers (pinned memory lets the copies overlap; pageable memory is correct
+ * but serialises them); o_host: [B,H,N,d] host output; perm, idx, residual: the
+ * meta-cache in device memory as for mcs_sparse_attn_gather. The B*H heads are
+ * split into head_chunks chunks (at most one per head): chunk c is copied in on
+ * a copy stream, computed on `stream`, and copied out on a second copy stream,
+ * so the copies of neighbouring chunks overlap the kernel; two chunks are staged
+ * in ws (device, 16-byte aligned, at least
+ * mcs_sparse_attn_gather_host_workspace_size(desc, head_chunks) bytes). Work is
+ * ordered after earlier work on `stream`, and `stream` is ordered after all of
+ * it (synchronise `stream` before reading o_host). Errors: MCS_ERR_INVALID_ARG
+ * for a bad argument, MCS_ERR_WORKSPACE for a small or misaligned ws,
+ * MCS_ERR_CUDA if a stream, event or copy cannot be set up. */
+size_t mcs_sparse_attn_gather_host_workspace_size(const mcs_desc *desc, int head_chunks);
+mcs_status mcs_sparse_attn_gather_host(const mcs_desc *desc, const void *q_host, const void *k_host,
+                                       const void *v_host, const int32_t *perm, const int32_t *idx, int K,
+                                       const void *residual, void *o_host, void *ws, size_t ws_bytes,
+                                       int head_chunks, mcs_stream stream);
+
 /* [residual] anchor residual in one pass: the sparse attention of
  * mcs_sparse_attn_gather (without residual) is computed and r_i = o_dense_i -
  * o_sparse_i is written, in fp32 and rounded once to dtype. o_dense: [B,H,N,d]

@@ -317,6 +317,108 @@ mcs_status mcs_sparse_attn_gather(const mcs_desc* desc, const void* q, const voi
                      nullptr, status, reinterpret_cast<cudaStream_t>(stream));
 }
 
+namespace {
+// Heads per chunk and the 256-byte-rounded bytes of one staged tensor chunk.
+bool host_chunking(const Dims& dm, int head_chunks, int* nch, int* hpc, size_t* chunk_bytes) {
+  if (head_chunks < 1) return false;
+  *nch = head_chunks < dm.BH ? head_chunks : dm.BH;
+  *hpc = (dm.BH + *nch - 1) / *nch;
+  *nch = (dm.BH + *hpc - 1) / *hpc;
+  const size_t es = dm.bf16 ? 2 : 4;
+  *chunk_bytes = ((size_t(*hpc) * dm.N * dm.d * es) + 255) & ~size_t(255);
+  return true;
+}
+}  // namespace
+
+size_t mcs_sparse_attn_gather_host_workspace_size(const mcs_desc* desc, int head_chunks) {
+  Dims dm;
+  int nch = 0, hpc = 0;
+  size_t cb = 0;
+  if (check_desc(desc, &dm) != MCS_OK || !host_chunking(dm, head_chunks, &nch, &hpc, &cb)) return 0;
+  return 2 * 4 * cb;  // two slots of q, k, v, o
+}
+
+mcs_status mcs_sparse_attn_gather_host(const mcs_desc* desc, const void* q_host, const void* k_host,
+                                       const void* v_host, const int32_t* perm, const int32_t* idx, int K,
+                                       const void* residual, void* o_host, void* ws, size_t ws_bytes,
+                                       int head_chunks, mcs_stream stream) {
+  Dims dm;
+  mcs_status st = check_desc(desc, &dm);
+  if (st != MCS_OK) return st;
+  if (K < 1 || K > dm.N) return MCS_ERR_INVALID_ARG;
+  if (q_host == nullptr || k_host == nullptr || v_host == nullptr || o_host == nullptr) return MCS_ERR_INVALID_ARG;
+  if (!aligned16(perm) || !aligned16(idx) || !aligned16_or_null(residual)) return MCS_ERR_INVALID_ARG;
+  int nch = 0, hpc = 0;
+  size_t cb = 0;
+  if (!host_chunking(dm, head_chunks, &nch, &hpc, &cb)) return MCS_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned16(ws) || ws_bytes < 2 * 4 * cb) return MCS_ERR_WORKSPACE;
+  uint32_t* status = nullptr;
+  if ((st = device_state(&status, nullptr)) != MCS_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t es = dm.bf16 ? 2 : 4, head_bytes = size_t(dm.N) * dm.d * es;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  auto slot_ptr = [&](int slot, int t) { return w + (size_t(slot) * 4 + t) * cb; };  // t: q, k, v, o
+  // copy-in and copy-out streams and the events that order the three streams;
+  // destroying them right after enqueueing is safe (released once the work ends)
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, end = nullptr, ev_in[2] = {}, ev_done[2] = {}, ev_free[2] = {};
+  auto cleanup = [&]() {
+    for (int i = 0; i < 2; ++i) {
+      if (ev_in[i]) cudaEventDestroy(ev_in[i]);
+      if (ev_done[i]) cudaEventDestroy(ev_done[i]);
+      if (ev_free[i]) cudaEventDestroy(ev_free[i]);
+    }
+    if (start) cudaEventDestroy(start);
+    if (end) cudaEventDestroy(end);
+    if (h2d) cudaStreamDestroy(h2d);
+    if (d2h) cudaStreamDestroy(d2h);
+  };
+  bool okc = cudaStreamCreateWithFlags(&h2d, cudaStreamNonBlocking) == cudaSuccess &&
+             cudaStreamCreateWithFlags(&d2h, cudaStreamNonBlocking) == cudaSuccess &&
+             cudaEventCreateWithFlags(&start, cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&end, cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; okc && i < 2; ++i)
+    okc = cudaEventCreateWithFlags(&ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
+          cudaEventCreateWithFlags(&ev_done[i], cudaEventDisableTiming) == cudaSuccess &&
+          cudaEventCreateWithFlags(&ev_free[i], cudaEventDisableTiming) == cudaSuccess;
+  okc = okc && cudaEventRecord(start, s) == cudaSuccess && cudaStreamWaitEvent(h2d, start, 0) == cudaSuccess &&
+        cudaStreamWaitEvent(d2h, start, 0) == cudaSuccess;
+  for (int c = 0; okc && c < nch; ++c) {
+    const int slot = c & 1, bh0 = c * hpc, nh = (dm.BH - bh0) < hpc ? (dm.BH - bh0) : hpc;
+    const size_t off = size_t(bh0) * head_bytes, bytes = size_t(nh) * head_bytes;
+    // slot reuse: chunk c - 2's output has been copied out (after its kernel)
+    if (c >= 2) okc = cudaStreamWaitEvent(h2d, ev_free[slot], 0) == cudaSuccess;
+    okc = okc &&
+          cudaMemcpyAsync(slot_ptr(slot, 0), static_cast<const uint8_t*>(q_host) + off, bytes, cudaMemcpyHostToDevice,
+                          h2d) == cudaSuccess &&
+          cudaMemcpyAsync(slot_ptr(slot, 1), static_cast<const uint8_t*>(k_host) + off, bytes, cudaMemcpyHostToDevice,
+                          h2d) == cudaSuccess &&
+          cudaMemcpyAsync(slot_ptr(slot, 2), static_cast<const uint8_t*>(v_host) + off, bytes, cudaMemcpyHostToDevice,
+                          h2d) == cudaSuccess &&
+          cudaEventRecord(ev_in[slot], h2d) == cudaSuccess && cudaStreamWaitEvent(s, ev_in[slot], 0) == cudaSuccess;
+    if (!okc) break;
+    Dims dc = dm;
+    dc.B = 1;
+    dc.H = nh;
+    dc.BH = nh;
+    const void* rc = residual ? static_cast<const uint8_t*>(residual) + off : nullptr;
+    st = sparse_impl(dc, residual ? mcs::kEpiAddResidual : mcs::kEpiPlain, slot_ptr(slot, 0), slot_ptr(slot, 1),
+                     slot_ptr(slot, 2), perm + size_t(bh0) * dm.N_pad, idx + size_t(bh0) * dm.G * size_t(K), K, rc,
+                     slot_ptr(slot, 3), nullptr, status, s);
+    if (st != MCS_OK) break;
+    okc = cudaEventRecord(ev_done[slot], s) == cudaSuccess && cudaStreamWaitEvent(d2h, ev_done[slot], 0) == cudaSuccess &&
+          cudaMemcpyAsync(static_cast<uint8_t*>(o_host) + off, slot_ptr(slot, 3), bytes, cudaMemcpyDeviceToHost, d2h) ==
+              cudaSuccess &&
+          cudaEventRecord(ev_free[slot], d2h) == cudaSuccess;
+  }
+  // the caller's stream completes after every copy
+  if (okc && st == MCS_OK)
+    okc = cudaEventRecord(end, d2h) == cudaSuccess && cudaStreamWaitEvent(s, end, 0) == cudaSuccess;
+  cleanup();
+  if (st != MCS_OK) return st;
+  return okc ? MCS_OK : MCS_ERR_CUDA;
+}
+
 mcs_status mcs_anchor_residual(const mcs_desc* desc, const void* q, const void* k, const void* v, const int32_t* perm,
                                const int32_t* idx, int K, const void* o_dense, void* r, mcs_stream stream) {
   Dims dm;

@@ -23,7 +23,8 @@ MCS_F32, MCS_BF16 = 0, 1
 EXPORTS = ("mcs_workspace_size", "mcs_group_pddp", "mcs_dense_attn", "mcs_anchor_select",
            "mcs_sparse_attn_gather", "mcs_anchor_residual", "mcs_residual_store", "mcs_residual_apply",
            "mcs_check_status", "mcs_status_string", "mcs_launch_count", "mcs_selftest_tc_mma",
-           "mcs_selftest_tma_gather", "mcs_anchor_select_noalloc")
+           "mcs_selftest_tma_gather", "mcs_anchor_select_noalloc", "mcs_sparse_attn_gather_host",
+           "mcs_sparse_attn_gather_host_workspace_size")
 
 
 class McsError(RuntimeError):
@@ -72,6 +73,8 @@ def load(build_if_missing: bool = False):
         "mcs_selftest_tc_mma": (I, [P, P, P, I, ctypes.c_uint32, ctypes.c_uint32, S]),
         "mcs_selftest_tma_gather": (I, [P, I, P, P, S]),
         "mcs_anchor_select_noalloc": (I, [D, P, P, P, P, I, P, P, S]),
+        "mcs_sparse_attn_gather_host": (I, [D, P, P, P, P, P, I, P, P, P, Z, I, S]),
+        "mcs_sparse_attn_gather_host_workspace_size": (Z, [D, I]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -160,6 +163,30 @@ def mcs_sparse_attn_gather(desc, q, k, v, perm, idx, K, residual, o, stream=None
     _check("mcs_sparse_attn_gather", load().mcs_sparse_attn_gather(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v),
                                                                    _ptr(perm), _ptr(idx), int(K), _ptr(residual),
                                                                    _ptr(o), _stream(stream)))
+
+
+def _host_ptr(t):
+    if t.is_cuda:
+        raise ValueError("expected a host tensor")
+    if not t.is_contiguous():
+        raise ValueError("libmcs takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def host_gather_workspace(desc, head_chunks, device="cuda") -> torch.Tensor:
+    n = load().mcs_sparse_attn_gather_host_workspace_size(ctypes.byref(desc), int(head_chunks))
+    if n == 0:
+        raise McsError("mcs_sparse_attn_gather_host_workspace_size", 1)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def mcs_sparse_attn_gather_host(desc, q_host, k_host, v_host, perm, idx, K, residual, o_host, ws, head_chunks,
+                                stream=None):
+    """Reuse-step sparse attention from host q/k/v (pinned for overlap) to a host output."""
+    _check("mcs_sparse_attn_gather_host", load().mcs_sparse_attn_gather_host(
+        ctypes.byref(desc), _host_ptr(q_host), _host_ptr(k_host), _host_ptr(v_host), _ptr(perm), _ptr(idx), int(K),
+        _ptr(residual), _host_ptr(o_host), _ptr(ws), ws.numel() * ws.element_size(), int(head_chunks),
+        _stream(stream)))
 
 
 def mcs_anchor_residual(desc, q, k, v, perm, idx, K, o_dense, r, stream=None):

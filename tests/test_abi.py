@@ -86,3 +86,23 @@ def test_launch_counter_is_monotone(lib):
     d = _desc(d=96)
     lib.mcs_dense_attn(ctypes.byref(d), None, None, None, None, None, None)
     assert lib.mcs_launch_count() == c0          # a rejected call launches nothing
+
+
+def test_host_gather_validation(lib):
+    d = _desc()                                   # B=1, H=2, N=600, d=128, bf16
+    one = lib.mcs_sparse_attn_gather_host_workspace_size(ctypes.byref(d), 1)
+    assert one == 2 * 4 * (((2 * 600 * 128 * 2) + 255) // 256 * 256)    # two slots of q, k, v, o
+    two = lib.mcs_sparse_attn_gather_host_workspace_size(ctypes.byref(d), 2)
+    assert two == 2 * 4 * (((600 * 128 * 2) + 255) // 256 * 256)
+    assert lib.mcs_sparse_attn_gather_host_workspace_size(ctypes.byref(d), 9) == two   # at most one chunk per head
+    assert lib.mcs_sparse_attn_gather_host_workspace_size(ctypes.byref(d), 0) == 0
+    assert lib.mcs_sparse_attn_gather_host_workspace_size(ctypes.byref(_desc(d=96)), 1) == 0
+    a = ctypes.c_void_p(4096)
+    g = lib.mcs_sparse_attn_gather_host
+    assert g(ctypes.byref(d), None, a, a, a, a, 10, None, a, a, one, 1, None) == 1       # no q
+    assert g(ctypes.byref(d), a, a, a, a, a, 10, None, None, a, one, 1, None) == 1       # no output
+    assert g(ctypes.byref(d), a, a, a, a, a, 0, None, a, a, one, 1, None) == 1           # K < 1
+    assert g(ctypes.byref(d), a, a, a, a, a, 10, None, a, a, one, 0, None) == 1          # no chunks
+    assert g(ctypes.byref(d), a, a, a, a, a, 10, None, a, a, one - 1, 1, None) == 3      # small workspace
+    assert g(ctypes.byref(d), a, a, a, a, a, 10, None, a, None, one, 1, None) == 3       # no workspace
+    assert g(ctypes.byref(d), a, a, a, a, a, 10, None, a, ctypes.c_void_p(4104), one, 1, None) == 3
