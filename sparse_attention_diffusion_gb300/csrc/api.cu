@@ -195,8 +195,10 @@ mcs_status mcs_group_pddp(const mcs_desc* desc, const void* q, int32_t* perm, in
   if (!aligned16(q) || !aligned16(perm) || !aligned16(group_of)) return MCS_ERR_INVALID_ARG;
   if (ws == nullptr || !aligned16(ws) || ws_bytes < mcs_workspace_size(desc, 1)) return MCS_ERR_WORKSPACE;
   uint32_t* status = nullptr;
-  if ((st = device_state(&status, nullptr)) != MCS_OK) return st;
+  int sms = 0;
+  if ((st = device_state(&status, &sms)) != MCS_OK) return st;
   mcs::PddpProblem p{};
+  p.num_sms = sms;
   p.q = q;
   p.perm = perm;
   p.group_of = group_of;

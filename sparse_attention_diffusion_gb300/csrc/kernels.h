@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace mcs {
@@ -30,11 +31,18 @@ struct PddpProblem {
   int32_t* group_of;     // [BH, N] output
   int BH, N, N_pad, C, G, d, iters;
   bool bf16;
+  int num_sms;
   uint32_t* status;
 };
 // Workspace bytes for pddp_run (0 if unsupported).
 size_t pddp_workspace_bytes(int BH, int N_pad, int C, int G, int d, bool bf16);
 cudaError_t pddp_run(const PddpProblem& p, void* ws, size_t ws_bytes, cudaStream_t stream);
+// Tensor-core chunk moments of one PDDP level (bf16, d = 128): per (head, chunk)
+// the raw second moment sum x x^T [d x d], the sum of x [d] and the real-row
+// count, for the chunks' rows gathered through perm (pddp_tc.cu).
+cudaError_t pddp_moments_tc(const __nv_bfloat16* x, const int32_t* perm, const int* chunk_g0, const int* chunk_ng,
+                            int nch, int BH, int N, int N_pad, int C, float* psum, int* pcnt, float* pcov,
+                            int max_chunks, uint32_t* status, int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------------- fp32 SIMT attention
 struct SimtAttnParams {

@@ -15,8 +15,12 @@
 //   5. radix-selects the rank floor(n/2)*C key of each node and stably
 //      partitions the run: smaller keys (ties: earlier, i.e. lower token id) left.
 // All reductions run in a fixed order, so a run is deterministic. fp32 inputs
-// accumulate in fp64 end to end; bf16 inputs accumulate in fp32.
+// accumulate in fp64 end to end; bf16 inputs accumulate in fp32. For bf16 at
+// d = 128, steps 1 and 2 are one tensor-core pass (pddp_tc.cu) giving each
+// chunk's sum and raw second moment sum x x^T; the node covariance is then
+// their fixed-order sum minus n mu mu^T.
 #include <cmath>
+#include <type_traits>
 #include <vector>
 
 #include "block_scan.cuh"
@@ -291,9 +295,11 @@ __global__ void __launch_bounds__(256) cov_kernel(const T* __restrict__ x, const
 }
 
 // 3b. node covariance (fixed-order sum of its chunks) and the power iterations.
-template <typename A, int D>
+// kRaw: the chunks hold raw second moments (tensor-core path), so the node's
+// n mu mu^T is subtracted once here.
+template <typename A, int D, bool kRaw>
 __global__ void __launch_bounds__(256) power_kernel(Tables t, int level, int G, const A* pcov, A* node_v, int iters,
-                                                    int max_chunks) {
+                                                    int max_chunks, const A* node_mu, const int* pcnt) {
   extern __shared__ uint8_t dyn[];
   A* cov = reinterpret_cast<A*>(dyn);  // [D][D]
   A* v = cov + D * D;                  // [D]
@@ -303,11 +309,18 @@ __global__ void __launch_bounds__(256) power_kernel(Tables t, int level, int G, 
   const size_t to = size_t(level) * G + k;
   if (t.node_n[to] < 2) return;
   const int c0 = t.node_chunk0[to], nc = t.node_nchunks[to];
+  if (kRaw && threadIdx.x < D) w[threadIdx.x] = node_mu[(size_t(bh) * G + k) * D + threadIdx.x];
+  int cnt = 0;
+  if (kRaw)
+    for (int c = 0; c < nc; ++c) cnt += pcnt[size_t(bh) * max_chunks + c0 + c];
+  __syncthreads();
   for (int e = threadIdx.x; e < D * D; e += blockDim.x) {
     A s = 0;
     for (int c = 0; c < nc; ++c) s += pcov[(size_t(bh) * max_chunks + c0 + c) * D * D + e];
+    if (kRaw) s -= (A(cnt) * w[e / D]) * w[e % D];
     cov[e] = s;
   }
+  __syncthreads();
   if (threadIdx.x < D) v[threadIdx.x] = node_v[(size_t(bh) * G + k) * D + threadIdx.x];
   __syncthreads();
   for (int it = 0; it < iters; ++it) {
@@ -519,8 +532,11 @@ cudaError_t run_typed(const PddpProblem& p, uint8_t* ws, cudaStream_t s) {
     tables_kernel<<<w.L, 1024, 0, s>>>(t, G);
     ++nlaunch;
   }
+  // bf16 at d = 128: chunk moments on the tensor cores (raw second moments)
+  constexpr bool kTc = std::is_same<T, __nv_bfloat16>::value && D == 128;
   const int power_smem = int((D * D + 2 * D) * sizeof(A));
-  cudaError_t e = cudaFuncSetAttribute(power_kernel<A, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, power_smem);
+  cudaError_t e = cudaFuncSetAttribute(power_kernel<A, D, kTc>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       power_smem);
   if (e != cudaSuccess) return e;
   for (int l = 0; l < w.L; ++l) {
     const int nodes = 1 << l;
@@ -528,15 +544,24 @@ cudaError_t run_typed(const PddpProblem& p, uint8_t* ws, cudaStream_t s) {
     const dim3 gc(nch, p.BH), gn(nodes, p.BH);
     int32_t* cur = bufs[l & 1];
     int32_t* nxt = bufs[(l + 1) & 1];
-    sum_kernel<T, A, D><<<gc, 256, 0, s>>>(x, cur, t, l, p.N, p.N_pad, p.C, G, psum, pcnt, w.max_chunks);
-    mean_kernel<A, D><<<gn, D, 0, s>>>(t, l, G, psum, pcnt, node_mu, node_v, w.max_chunks);
-    cov_kernel<T, A, D><<<gc, 256, 0, s>>>(x, cur, t, l, p.N, p.N_pad, p.C, G, node_mu, pcov, w.max_chunks);
-    power_kernel<A, D><<<gn, 256, power_smem, s>>>(t, l, G, pcov, node_v, p.iters, w.max_chunks);
+    if constexpr (kTc) {
+      e = pddp_moments_tc(x, cur, t.chunk_g0 + size_t(l) * G, t.chunk_ng + size_t(l) * G, nch, p.BH, p.N, p.N_pad,
+                          p.C, psum, pcnt, pcov, w.max_chunks, p.status, p.num_sms, s);
+      if (e != cudaSuccess) return e;
+      mean_kernel<A, D><<<gn, D, 0, s>>>(t, l, G, psum, pcnt, node_mu, node_v, w.max_chunks);
+      nlaunch += 1;
+    } else {
+      sum_kernel<T, A, D><<<gc, 256, 0, s>>>(x, cur, t, l, p.N, p.N_pad, p.C, G, psum, pcnt, w.max_chunks);
+      mean_kernel<A, D><<<gn, D, 0, s>>>(t, l, G, psum, pcnt, node_mu, node_v, w.max_chunks);
+      cov_kernel<T, A, D><<<gc, 256, 0, s>>>(x, cur, t, l, p.N, p.N_pad, p.C, G, node_mu, pcov, w.max_chunks);
+      nlaunch += 3;
+    }
+    power_kernel<A, D, kTc><<<gn, 256, power_smem, s>>>(t, l, G, pcov, node_v, p.iters, w.max_chunks, node_mu, pcnt);
     keys_kernel<T, A, D, KeyT><<<gc, 256, 0, s>>>(x, cur, t, l, p.N, p.N_pad, p.C, G, node_mu, node_v, keys);
     e = cudaMemcpyAsync(nxt, cur, total * sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
     if (e != cudaSuccess) return e;
     split_kernel<KeyT><<<gn, 1024, 0, s>>>(cur, nxt, keys, t, l, p.N_pad, p.C, G, p.status);
-    nlaunch += 6;
+    nlaunch += 3;
   }
   finalize_kernel<<<1024, 256, 0, s>>>(p.perm, p.group_of, p.N, p.N_pad, p.C, total, p.status);
   ++nlaunch;
