@@ -17,6 +17,9 @@ runs once to report the total time including anchors and the anchor overhead as
 equivalent extra density (`anchor_overhead`; `--no-schedule` skips it), and the
 65,536-token density/tile sweep (d and C in {64, 128}, densities 0.05-1.0) reports
 the sparse kernel against the dense kernel per point (`sweep`; `--no-sweep`).
+It also times the reuse step with the meta-cache kept in pinned host memory
+through the cache ring (three layers' entries, the next one prefetched while
+the current one computes; `cache_ring`; `--no-ring` skips it).
 `--impl reference` times the float64 CPU oracle instead, on a bounded sample of
 groups, extrapolated to ms/layer.
 """
@@ -55,6 +58,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-schedule", action="store_true", help="skip the 118,800-token schedule (anchor overhead)")
     ap.add_argument("--no-sweep", action="store_true", help="skip the 65,536-token density/tile sweep")
+    ap.add_argument("--no-ring", action="store_true", help="skip the host-resident meta-cache (cache ring) timing")
     ap.add_argument("--heads", type=int, default=None, help="override H (smaller case for profiler captures)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget (CPU seconds)")
     ap.add_argument("--e2e-chunks", type=int, default=40, help="head chunks of the host-buffer reuse step (one head each by default)")
@@ -191,6 +195,47 @@ def run_reference(args, wl, K):
 
 
 # ---------------------------------------------------------------- GPU arm
+RING_LAYERS = 3
+
+
+def cache_ring_timing(desc, K, q, k, v, cache, stream):
+    """Reuse steps whose meta-cache lives in pinned host memory: RING_LAYERS
+    entries (copies of this layer's anchor cache, written out through the ring
+    as an anchor step would), then rounds over the layers where each layer's
+    entry is already resident from the previous layer's prefetch and the next
+    one is copied in during its kernel. Returns ms per layer of the second
+    round (device events on the compute stream)."""
+    import torch
+
+    from sparse_attention_diffusion_gb300 import mcs
+    ring = mcs.CacheRing(desc, K, RING_LAYERS, q.dtype)
+    o = torch.empty_like(q)
+    try:
+        for l in range(RING_LAYERS):
+            c = ring.acquire(l, fill=False, prefetch_next=False, stream=stream)
+            for key in ("perm", "idx", "residual"):
+                c[key].copy_(cache[key])
+            ring.release(l, store=True, stream=stream)
+        per_round = []
+        for _ in range(2):
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for l in range(RING_LAYERS):
+                c = ring.acquire(l, fill=True, prefetch_next=True, stream=stream)
+                mcs.mcs_sparse_attn_gather(desc, q, k, v, c["perm"], c["idx"], K, c["residual"], o, stream)
+                ring.release(l, stream=stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            per_round.append(a.elapsed_time(b) / RING_LAYERS)
+        mcs.mcs_check_status()
+        return {"ms_per_layer": per_round[-1], "first_round_ms_per_layer": per_round[0],
+                "entry_bytes": ring.entry, "layers": RING_LAYERS,
+                "note": "perm+idx+residual per layer in pinned host memory, two device slots; round 2 timed"}
+    finally:
+        ring.close()
+
+
 def schedule_overhead(dev):
     """The full meta-cache schedule on the 118,800-token layer (24 heads, 50 steps:
     5 dense warm-up steps, an anchor every 10 steps, reuse steps otherwise, drift
@@ -425,6 +470,10 @@ def run_mcs(args, wl, K):
                     "calls_ms": [round(x, 3) for x in e2e_calls], "stat": "median of 5 calls"},
             "clocks": clocks,
         }
+        if world == 1 and not args.no_ring:
+            ring = cache_ring_timing(desc, K, q2, k2, v2, cache, stream)
+            ring["resident_ms_per_layer"] = sparse_ms
+            line["cache_ring"] = ring
         if world == 1 and not args.no_schedule:
             line["anchor_overhead"] = schedule_overhead(dev)
         if world == 1 and not args.no_sweep:

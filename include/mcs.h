@@ -158,6 +158,46 @@ mcs_status mcs_sparse_attn_gather_host(const mcs_desc *desc, const void *q_host,
                                        const void *residual, void *o_host, void *ws, size_t ws_bytes,
                                        int head_chunks, mcs_stream stream);
 
+/* Meta-cache ring: the per-layer cache {perm, idx, residual} of a model's
+ * layers kept in HOST memory, with two device slots that take turns, so that a
+ * layer's entry is copied in while the previous layer computes and a fresh
+ * anchor entry is copied out while the next layer computes ([residual]: the
+ * cache is reused across steps; holding it for every layer is what fills device
+ * memory). All copies run on a stream the ring owns; compute on the caller's
+ * stream is ordered against them with events, so nothing blocks the host.
+ *
+ * One entry is perm [B,H,N_pad] int32, idx [B,H,G,K] int32 and residual
+ * [B,H,N,d] in the I/O dtype, each section 256-byte aligned, in
+ * mcs_cache_entry_bytes(desc, K) bytes. host_entries: n_layers entries in host
+ * memory (pinned for overlap), 256-byte aligned; device_slots: 2 entries in
+ * device memory, 256-byte aligned; both owned by the caller and valid until
+ * mcs_cache_ring_destroy returns. The ring is bound to the current device.
+ *
+ * mcs_cache_ring_acquire(layer, load, prefetch_next, stream, &perm, &idx,
+ *   &residual): returns device pointers to the layer's slot. load = 1 makes
+ *   the host entry resident first (nothing is copied when the slot already
+ *   holds it, e.g. from a prefetch); load = 0 only reserves a slot, for an
+ *   anchor step that will overwrite it. Work enqueued on `stream` afterwards
+ *   sees the slot's contents. prefetch_next = 1 also starts copying layer
+ *   (layer + 1) mod n_layers into the other slot, behind that slot's last
+ *   release (skipped while the other slot is acquired or already holds it).
+ *   At most two layers are acquired at once; a layer cannot be acquired twice.
+ * mcs_cache_ring_release(layer, store, stream): the layer's kernels on
+ *   `stream` are the last users of its slot; store = 1 then copies the slot
+ *   back to the layer's host entry (after those kernels).
+ * mcs_cache_ring_destroy: waits for the ring's copies, frees the ring.
+ * Errors: MCS_ERR_INVALID_ARG for a bad argument or an acquire/release out of
+ * order, MCS_ERR_CUDA if a stream, event or copy call fails. Calls on one ring
+ * are serialised by a lock. */
+typedef struct mcs_cache_ring_s *mcs_cache_ring;
+size_t mcs_cache_entry_bytes(const mcs_desc *desc, int K);
+mcs_status mcs_cache_ring_create(const mcs_desc *desc, int K, int n_layers, void *host_entries,
+                                 void *device_slots, mcs_cache_ring *ring);
+mcs_status mcs_cache_ring_acquire(mcs_cache_ring ring, int layer, int load, int prefetch_next,
+                                  mcs_stream stream, int32_t **perm, int32_t **idx, void **residual);
+mcs_status mcs_cache_ring_release(mcs_cache_ring ring, int layer, int store, mcs_stream stream);
+mcs_status mcs_cache_ring_destroy(mcs_cache_ring ring);
+
 /* [residual] anchor residual in one pass: the sparse attention of
  * mcs_sparse_attn_gather (without residual) is computed and r_i = o_dense_i -
  * o_sparse_i is written, in fp32 and rounded once to dtype. o_dense: [B,H,N,d]

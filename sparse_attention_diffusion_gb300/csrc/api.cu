@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "mcs.h"
 #include "attn_tc.h"
@@ -510,3 +511,157 @@ mcs_status mcs_selftest_tma_gather(const void* src, int nrows, const int32_t* ro
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- meta-cache ring
+// One layer's entry: perm [BH, N_pad] int32 | idx [BH, G, K] int32 | residual
+// [BH, N, d], each section starting on a 256-byte boundary. Two device slots
+// take turns: the layer being computed sits in one while the next one is copied
+// into the other on the ring's copy stream. Per slot, `copied` (recorded on the
+// copy stream after every copy touching the slot) orders compute after copies,
+// and `used` (recorded on the compute stream when the layer is released) orders
+// copies after compute.
+namespace {
+struct EntryLayout {
+  size_t perm, idx, res, total;
+  size_t perm_bytes, idx_bytes, res_bytes;
+};
+EntryLayout entry_layout(const Dims& dm, int K) {
+  EntryLayout e{};
+  e.perm_bytes = size_t(dm.BH) * dm.N_pad * 4;
+  e.idx_bytes = size_t(dm.BH) * dm.G * size_t(K) * 4;
+  e.res_bytes = size_t(dm.BH) * dm.N * dm.d * (dm.bf16 ? 2 : 4);
+  e.perm = 0;
+  e.idx = align256(e.perm + e.perm_bytes);
+  e.res = align256(e.idx + e.idx_bytes);
+  e.total = align256(e.res + e.res_bytes);
+  return e;
+}
+}  // namespace
+
+struct mcs_cache_ring_s {
+  Dims dm;
+  int K = 0, n_layers = 0, device = 0;
+  EntryLayout lay{};
+  uint8_t* host = nullptr;  // [n_layers] entries, pinned (caller's)
+  uint8_t* dev = nullptr;   // [2] slots (caller's)
+  cudaStream_t copy = nullptr;
+  cudaEvent_t copied[2] = {}, used[2] = {};
+  int holds[2] = {-1, -1};  // layer whose entry the slot holds (or receives, once `copied` completes)
+  int last = 1;             // slot of the most recent acquire
+  int current[2] = {-1, -1};  // layer acquired into the slot and not yet released
+  std::mutex mu;
+};
+
+namespace {
+void ring_free(mcs_cache_ring r) {
+  for (int i = 0; i < 2; ++i) {
+    if (r->copied[i]) cudaEventDestroy(r->copied[i]);
+    if (r->used[i]) cudaEventDestroy(r->used[i]);
+  }
+  if (r->copy) cudaStreamDestroy(r->copy);
+  delete r;
+}
+bool ring_copy(mcs_cache_ring r, int slot, int layer, bool to_device) {
+  uint8_t* d = r->dev + size_t(slot) * r->lay.total;
+  uint8_t* h = r->host + size_t(layer) * r->lay.total;
+  const cudaMemcpyKind kind = to_device ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToHost;
+  // copy after the slot's last compute use, then mark the slot's copies done
+  if (cudaStreamWaitEvent(r->copy, r->used[slot], 0) != cudaSuccess) return false;
+  const size_t off[3] = {r->lay.perm, r->lay.idx, r->lay.res};
+  const size_t len[3] = {r->lay.perm_bytes, r->lay.idx_bytes, r->lay.res_bytes};
+  for (int t = 0; t < 3; ++t) {
+    void* dst = to_device ? static_cast<void*>(d + off[t]) : static_cast<void*>(h + off[t]);
+    const void* src = to_device ? static_cast<const void*>(h + off[t]) : static_cast<const void*>(d + off[t]);
+    if (cudaMemcpyAsync(dst, src, len[t], kind, r->copy) != cudaSuccess) return false;
+  }
+  return cudaEventRecord(r->copied[slot], r->copy) == cudaSuccess;
+}
+}  // namespace
+
+size_t mcs_cache_entry_bytes(const mcs_desc* desc, int K) {
+  Dims dm;
+  if (check_desc(desc, &dm) != MCS_OK || K < 1 || K > dm.N) return 0;
+  return entry_layout(dm, K).total;
+}
+
+mcs_status mcs_cache_ring_create(const mcs_desc* desc, int K, int n_layers, void* host_entries, void* device_slots,
+                                 mcs_cache_ring* out) {
+  if (out == nullptr) return MCS_ERR_INVALID_ARG;
+  *out = nullptr;
+  Dims dm;
+  mcs_status st = check_desc(desc, &dm);
+  if (st != MCS_OK) return st;
+  if (K < 1 || K > dm.N || n_layers < 1) return MCS_ERR_INVALID_ARG;
+  if (host_entries == nullptr || (reinterpret_cast<uintptr_t>(host_entries) & 255u) != 0) return MCS_ERR_INVALID_ARG;
+  if (device_slots == nullptr || (reinterpret_cast<uintptr_t>(device_slots) & 255u) != 0) return MCS_ERR_INVALID_ARG;
+  mcs_cache_ring r = new (std::nothrow) mcs_cache_ring_s();
+  if (r == nullptr) return MCS_ERR_INVALID_ARG;
+  r->dm = dm;
+  r->K = K;
+  r->n_layers = n_layers;
+  r->lay = entry_layout(dm, K);
+  r->host = static_cast<uint8_t*>(host_entries);
+  r->dev = static_cast<uint8_t*>(device_slots);
+  bool ok = cudaGetDevice(&r->device) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&r->copy, cudaStreamNonBlocking) == cudaSuccess;
+  for (int i = 0; ok && i < 2; ++i)
+    ok = cudaEventCreateWithFlags(&r->copied[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&r->used[i], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    ring_free(r);
+    return MCS_ERR_CUDA;
+  }
+  *out = r;
+  return MCS_OK;
+}
+
+mcs_status mcs_cache_ring_acquire(mcs_cache_ring r, int layer, int load, int prefetch_next, mcs_stream stream,
+                                  int32_t** perm, int32_t** idx, void** residual) {
+  if (r == nullptr || layer < 0 || layer >= r->n_layers || perm == nullptr || idx == nullptr || residual == nullptr)
+    return MCS_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(r->mu);
+  if (r->current[0] == layer || r->current[1] == layer) return MCS_ERR_INVALID_ARG;  // already acquired
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the slot that holds (or is receiving) this layer, else the one not acquired last
+  int slot = r->holds[0] == layer ? 0 : (r->holds[1] == layer ? 1 : (r->last ^ 1));
+  if (r->current[slot] >= 0) return MCS_ERR_INVALID_ARG;  // both slots in use: release first
+  if (load && r->holds[slot] != layer) {
+    if (!ring_copy(r, slot, layer, true)) return MCS_ERR_CUDA;
+  }
+  r->holds[slot] = layer;  // the caller overwrites it when load == 0
+  if (cudaStreamWaitEvent(s, r->copied[slot], 0) != cudaSuccess) return MCS_ERR_CUDA;
+  r->current[slot] = layer;
+  r->last = slot;
+  if (prefetch_next && r->n_layers > 1) {
+    const int nl = (layer + 1) % r->n_layers, ns = slot ^ 1;
+    if (r->current[ns] < 0 && r->holds[ns] != nl) {
+      if (!ring_copy(r, ns, nl, true)) return MCS_ERR_CUDA;
+      r->holds[ns] = nl;
+    }
+  }
+  uint8_t* d = r->dev + size_t(slot) * r->lay.total;
+  *perm = reinterpret_cast<int32_t*>(d + r->lay.perm);
+  *idx = reinterpret_cast<int32_t*>(d + r->lay.idx);
+  *residual = d + r->lay.res;
+  return MCS_OK;
+}
+
+mcs_status mcs_cache_ring_release(mcs_cache_ring r, int layer, int store, mcs_stream stream) {
+  if (r == nullptr || layer < 0 || layer >= r->n_layers) return MCS_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(r->mu);
+  const int slot = r->current[0] == layer ? 0 : (r->current[1] == layer ? 1 : -1);
+  if (slot < 0) return MCS_ERR_INVALID_ARG;  // not acquired
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaEventRecord(r->used[slot], s) != cudaSuccess) return MCS_ERR_CUDA;
+  if (store && !ring_copy(r, slot, layer, false)) return MCS_ERR_CUDA;
+  r->current[slot] = -1;
+  return MCS_OK;
+}
+
+mcs_status mcs_cache_ring_destroy(mcs_cache_ring r) {
+  if (r == nullptr) return MCS_ERR_INVALID_ARG;
+  // the copies still queued read or write the caller's buffers: let them finish
+  const bool ok = cudaStreamSynchronize(r->copy) == cudaSuccess;
+  ring_free(r);
+  return ok ? MCS_OK : MCS_ERR_CUDA;
+}

@@ -24,7 +24,8 @@ EXPORTS = ("mcs_workspace_size", "mcs_group_pddp", "mcs_dense_attn", "mcs_anchor
            "mcs_sparse_attn_gather", "mcs_anchor_residual", "mcs_residual_store", "mcs_residual_apply",
            "mcs_check_status", "mcs_status_string", "mcs_launch_count", "mcs_selftest_tc_mma",
            "mcs_selftest_tma_gather", "mcs_anchor_select_noalloc", "mcs_sparse_attn_gather_host",
-           "mcs_sparse_attn_gather_host_workspace_size")
+           "mcs_sparse_attn_gather_host_workspace_size", "mcs_cache_entry_bytes", "mcs_cache_ring_create",
+           "mcs_cache_ring_acquire", "mcs_cache_ring_release", "mcs_cache_ring_destroy")
 
 
 class McsError(RuntimeError):
@@ -75,6 +76,12 @@ def load(build_if_missing: bool = False):
         "mcs_anchor_select_noalloc": (I, [D, P, P, P, P, I, P, P, S]),
         "mcs_sparse_attn_gather_host": (I, [D, P, P, P, P, P, I, P, P, P, Z, I, S]),
         "mcs_sparse_attn_gather_host_workspace_size": (Z, [D, I]),
+        "mcs_cache_entry_bytes": (Z, [D, I]),
+        "mcs_cache_ring_create": (I, [D, I, I, P, P, ctypes.POINTER(ctypes.c_void_p)]),
+        "mcs_cache_ring_acquire": (I, [P, I, I, I, S, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p),
+                                       ctypes.POINTER(ctypes.c_void_p)]),
+        "mcs_cache_ring_release": (I, [P, I, I, S]),
+        "mcs_cache_ring_destroy": (I, [P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -187,6 +194,56 @@ def mcs_sparse_attn_gather_host(desc, q_host, k_host, v_host, perm, idx, K, resi
         ctypes.byref(desc), _host_ptr(q_host), _host_ptr(k_host), _host_ptr(v_host), _ptr(perm), _ptr(idx), int(K),
         _ptr(residual), _host_ptr(o_host), _ptr(ws), ws.numel() * ws.element_size(), int(head_chunks),
         _stream(stream)))
+
+
+class CacheRing:
+    """The per-layer meta-cache {perm, idx, residual} of n_layers layers in pinned
+    host memory with two device slots (mcs_cache_ring_*). acquire() returns
+    device tensors viewing the layer's slot; they stay valid until release()."""
+
+    def __init__(self, desc, K, n_layers, dtype, device="cuda"):
+        lib = load()
+        self.desc, self.K, self.n_layers, self.dtype = desc, int(K), int(n_layers), dtype
+        self.entry = lib.mcs_cache_entry_bytes(ctypes.byref(desc), self.K)
+        if self.entry == 0:
+            raise McsError("mcs_cache_entry_bytes", 1)
+        self.host = torch.empty(self.n_layers * self.entry + 256, dtype=torch.uint8, pin_memory=True)
+        self.dev = torch.empty(2 * self.entry + 256, dtype=torch.uint8, device=device)
+        h = ctypes.c_void_p((self.host.data_ptr() + 255) & ~255)
+        d = ctypes.c_void_p((self.dev.data_ptr() + 255) & ~255)
+        self._h0, self._d0 = h.value, d.value
+        self._ring = ctypes.c_void_p()
+        _check("mcs_cache_ring_create", lib.mcs_cache_ring_create(ctypes.byref(desc), self.K, self.n_layers, h, d,
+                                                                  ctypes.byref(self._ring)))
+        G, N_pad = geometry(desc)
+        self._shapes = ((desc.B, desc.H, N_pad), (desc.B, desc.H, G, self.K), (desc.B, desc.H, desc.N, desc.d))
+
+    def _view(self, addr, shape, dtype):
+        n = 1
+        for s in shape:
+            n *= s
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        off = addr - self.dev.data_ptr()
+        return self.dev[off:off + nbytes].view(dtype).view(shape)
+
+    def acquire(self, layer, fill=True, prefetch_next=True, stream=None):
+        """fill: make the layer's host entry resident (False: the caller overwrites the slot)."""
+        p, i, r = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
+        _check("mcs_cache_ring_acquire", load().mcs_cache_ring_acquire(
+            self._ring, int(layer), int(bool(fill)), int(bool(prefetch_next)), _stream(stream), ctypes.byref(p),
+            ctypes.byref(i), ctypes.byref(r)))
+        sp, si, sr = self._shapes
+        return {"perm": self._view(p.value, sp, torch.int32), "idx": self._view(i.value, si, torch.int32),
+                "residual": self._view(r.value, sr, self.dtype)}
+
+    def release(self, layer, store=False, stream=None):
+        _check("mcs_cache_ring_release", load().mcs_cache_ring_release(self._ring, int(layer), int(bool(store)),
+                                                                         _stream(stream)))
+
+    def close(self):
+        if self._ring:
+            _check("mcs_cache_ring_destroy", load().mcs_cache_ring_destroy(self._ring))
+            self._ring = ctypes.c_void_p()
 
 
 def mcs_anchor_residual(desc, q, k, v, perm, idx, K, o_dense, r, stream=None):

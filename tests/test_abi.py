@@ -106,3 +106,24 @@ def test_host_gather_validation(lib):
     assert g(ctypes.byref(d), a, a, a, a, a, 10, None, a, a, one - 1, 1, None) == 3      # small workspace
     assert g(ctypes.byref(d), a, a, a, a, a, 10, None, a, None, one, 1, None) == 3       # no workspace
     assert g(ctypes.byref(d), a, a, a, a, a, 10, None, a, ctypes.c_void_p(4104), one, 1, None) == 3
+
+
+def test_cache_ring_validation(lib):
+    d = _desc()                                   # B=1, H=2, N=600 (N_pad 640, G 5), d=128, bf16
+    n = lib.mcs_cache_entry_bytes(ctypes.byref(d), 120)
+    a256 = lambda x: (x + 255) // 256 * 256
+    assert n == a256(2 * 640 * 4) + a256(2 * 5 * 120 * 4) + a256(2 * 600 * 128 * 2)
+    assert lib.mcs_cache_entry_bytes(ctypes.byref(d), 0) == 0
+    assert lib.mcs_cache_entry_bytes(ctypes.byref(d), 601) == 0
+    ring = ctypes.c_void_p()
+    a = ctypes.c_void_p(4096)
+    c = lib.mcs_cache_ring_create
+    assert c(ctypes.byref(d), 120, 0, a, a, ctypes.byref(ring)) == 1                     # no layers
+    assert c(ctypes.byref(d), 120, 3, None, a, ctypes.byref(ring)) == 1                  # no host entries
+    assert c(ctypes.byref(d), 120, 3, a, ctypes.c_void_p(4096 + 16), ctypes.byref(ring)) == 1  # slots not 256-aligned
+    assert c(ctypes.byref(d), 120, 3, a, a, None) == 1
+    assert c(ctypes.byref(_desc(d=96)), 120, 3, a, a, ctypes.byref(ring)) == 2
+    p = ctypes.c_void_p()
+    assert lib.mcs_cache_ring_acquire(None, 0, 1, 1, None, ctypes.byref(p), ctypes.byref(p), ctypes.byref(p)) == 1
+    assert lib.mcs_cache_ring_release(None, 0, 0, None) == 1
+    assert lib.mcs_cache_ring_destroy(None) == 1
