@@ -17,6 +17,10 @@ runs once to report the total time including anchors and the anchor overhead as
 equivalent extra density (`anchor_overhead`; `--no-schedule` skips it), and the
 65,536-token density/tile sweep (d and C in {64, 128}, densities 0.05-1.0) reports
 the sparse kernel against the dense kernel per point (`sweep`; `--no-sweep`).
+`matched_density` compares, on the same layer at its density, the captured
+attention mass and the sparse output's relative error (||R|| / ||O_dense||) of
+the group-shared selection with the PDDP groups against contiguous tile groups
+(`--no-matched` skips it).
 It also times the reuse step with the meta-cache kept in pinned host memory
 through the cache ring (three layers' entries, the next one prefetched while
 the current one computes; `cache_ring`; `--no-ring` skips it).
@@ -59,6 +63,7 @@ def parse():
     ap.add_argument("--no-schedule", action="store_true", help="skip the 118,800-token schedule (anchor overhead)")
     ap.add_argument("--no-sweep", action="store_true", help="skip the 65,536-token density/tile sweep")
     ap.add_argument("--no-ring", action="store_true", help="skip the host-resident meta-cache (cache ring) timing")
+    ap.add_argument("--no-matched", action="store_true", help="skip the PDDP-vs-contiguous group mass comparison")
     ap.add_argument("--heads", type=int, default=None, help="override H (smaller case for profiler captures)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget (CPU seconds)")
     ap.add_argument("--e2e-chunks", type=int, default=40, help="head chunks of the host-buffer reuse step (one head each by default)")
@@ -234,6 +239,33 @@ def cache_ring_timing(desc, K, q, k, v, cache, stream):
                 "note": "perm+idx+residual per layer in pinned host memory, two device slots; round 2 timed"}
     finally:
         ring.close()
+
+
+def matched_density(desc, K, q, k, v, o_dense, cache, ws):
+    """Group-shared selection on the benchmark layer with the PDDP groups (the
+    anchor's cache) and with contiguous tile groups (identity perm): mean captured
+    mass over groups and the anchor sparse output's relative error."""
+    import torch
+
+    from sparse_attention_diffusion_gb300 import mcs
+
+    def rel_err(R):
+        return float(torch.linalg.vector_norm(R.float()) / torch.linalg.vector_norm(o_dense.float()))
+
+    out = {"mass_group_pddp": float(cache["mass"].float().mean()), "rel_err_group_pddp": rel_err(cache["residual"])}
+    G, N_pad = mcs.geometry(desc)
+    perm = torch.arange(N_pad, dtype=torch.int32, device=q.device).expand_as(cache["perm"]).contiguous()
+    idx, mass = torch.empty_like(cache["idx"]), torch.empty_like(cache["mass"])
+    R = torch.empty_like(cache["residual"])
+    mcs.mcs_anchor_select(desc, q, k, perm, None, K, idx, mass, ws)
+    mcs.mcs_anchor_residual(desc, q, k, v, perm, idx, K, o_dense, R)
+    mcs.mcs_check_status()
+    out.update(mass_group_contiguous=float(mass.float().mean()), rel_err_group_contiguous=rel_err(R),
+               note="mean over groups of the captured fraction of dense attention mass; error of the sparse "
+                    "output before the residual")
+    del perm, idx, mass, R
+    torch.cuda.empty_cache()
+    return out
 
 
 def schedule_overhead(dev):
@@ -470,6 +502,8 @@ def run_mcs(args, wl, K):
                     "calls_ms": [round(x, 3) for x in e2e_calls], "stat": "median of 5 calls"},
             "clocks": clocks,
         }
+        if world == 1 and not args.no_matched:
+            line["matched_density"] = matched_density(desc, K, q, k, v, o_dense, cache, ws)
         if world == 1 and not args.no_ring:
             ring = cache_ring_timing(desc, K, q2, k2, v2, cache, stream)
             ring["resident_ms_per_layer"] = sparse_ms
