@@ -144,8 +144,10 @@ mcs_status mcs_sparse_attn_gather(const mcs_desc *desc, const void *q, const voi
  * but serialises them); o_host: [B,H,N,d] host output; perm, idx, residual: the
  * meta-cache in device memory as for mcs_sparse_attn_gather. The B*H heads are
  * split into head_chunks chunks (at most one per head): chunk c is copied in on
- * a copy stream, computed on `stream`, and copied out on a second copy stream,
- * so the copies of neighbouring chunks overlap the kernel; two chunks are staged
+ * a copy stream, computed on one of two internal streams (alternating, so that
+ * consecutive chunks' kernels overlap at their edges), and copied out on a
+ * second copy stream, so the copies of neighbouring chunks overlap the
+ * kernels; two chunks are staged
  * in ws (device, 16-byte aligned, at least
  * mcs_sparse_attn_gather_host_workspace_size(desc, head_chunks) bytes). Work is
  * ordered after earlier work on `stream`, and `stream` is ordered after all of

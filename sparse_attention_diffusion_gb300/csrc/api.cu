@@ -361,9 +361,11 @@ mcs_status mcs_sparse_attn_gather_host(const mcs_desc* desc, const void* q_host,
   const size_t es = dm.bf16 ? 2 : 4, head_bytes = size_t(dm.N) * dm.d * es;
   uint8_t* w = static_cast<uint8_t*>(ws);
   auto slot_ptr = [&](int slot, int t) { return w + (size_t(slot) * 4 + t) * cb; };  // t: q, k, v, o
-  // copy-in and copy-out streams and the events that order the three streams;
-  // destroying them right after enqueueing is safe (released once the work ends)
-  cudaStream_t h2d = nullptr, d2h = nullptr;
+  // copy-in and copy-out streams, two compute streams (even and odd chunks, so
+  // that a chunk's kernel fills the SMs its predecessor's last wave leaves idle)
+  // and the events that order them; destroying them right after enqueueing is
+  // safe (released once the work ends)
+  cudaStream_t h2d = nullptr, d2h = nullptr, cs[2] = {};
   cudaEvent_t start = nullptr, end = nullptr, ev_in[2] = {}, ev_done[2] = {}, ev_free[2] = {};
   auto cleanup = [&]() {
     for (int i = 0; i < 2; ++i) {
@@ -375,9 +377,13 @@ mcs_status mcs_sparse_attn_gather_host(const mcs_desc* desc, const void* q_host,
     if (end) cudaEventDestroy(end);
     if (h2d) cudaStreamDestroy(h2d);
     if (d2h) cudaStreamDestroy(d2h);
+    for (int i = 0; i < 2; ++i)
+      if (cs[i]) cudaStreamDestroy(cs[i]);
   };
   bool okc = cudaStreamCreateWithFlags(&h2d, cudaStreamNonBlocking) == cudaSuccess &&
              cudaStreamCreateWithFlags(&d2h, cudaStreamNonBlocking) == cudaSuccess &&
+             cudaStreamCreateWithFlags(&cs[0], cudaStreamNonBlocking) == cudaSuccess &&
+             cudaStreamCreateWithFlags(&cs[1], cudaStreamNonBlocking) == cudaSuccess &&
              cudaEventCreateWithFlags(&start, cudaEventDisableTiming) == cudaSuccess &&
              cudaEventCreateWithFlags(&end, cudaEventDisableTiming) == cudaSuccess;
   for (int i = 0; okc && i < 2; ++i)
@@ -385,7 +391,8 @@ mcs_status mcs_sparse_attn_gather_host(const mcs_desc* desc, const void* q_host,
           cudaEventCreateWithFlags(&ev_done[i], cudaEventDisableTiming) == cudaSuccess &&
           cudaEventCreateWithFlags(&ev_free[i], cudaEventDisableTiming) == cudaSuccess;
   okc = okc && cudaEventRecord(start, s) == cudaSuccess && cudaStreamWaitEvent(h2d, start, 0) == cudaSuccess &&
-        cudaStreamWaitEvent(d2h, start, 0) == cudaSuccess;
+        cudaStreamWaitEvent(d2h, start, 0) == cudaSuccess && cudaStreamWaitEvent(cs[0], start, 0) == cudaSuccess &&
+        cudaStreamWaitEvent(cs[1], start, 0) == cudaSuccess;
   for (int c = 0; okc && c < nch; ++c) {
     const int slot = c & 1, bh0 = c * hpc, nh = (dm.BH - bh0) < hpc ? (dm.BH - bh0) : hpc;
     const size_t off = size_t(bh0) * head_bytes, bytes = size_t(nh) * head_bytes;
@@ -398,7 +405,7 @@ mcs_status mcs_sparse_attn_gather_host(const mcs_desc* desc, const void* q_host,
                           h2d) == cudaSuccess &&
           cudaMemcpyAsync(slot_ptr(slot, 2), static_cast<const uint8_t*>(v_host) + off, bytes, cudaMemcpyHostToDevice,
                           h2d) == cudaSuccess &&
-          cudaEventRecord(ev_in[slot], h2d) == cudaSuccess && cudaStreamWaitEvent(s, ev_in[slot], 0) == cudaSuccess;
+          cudaEventRecord(ev_in[slot], h2d) == cudaSuccess && cudaStreamWaitEvent(cs[slot], ev_in[slot], 0) == cudaSuccess;
     if (!okc) break;
     Dims dc = dm;
     dc.B = 1;
@@ -407,14 +414,15 @@ mcs_status mcs_sparse_attn_gather_host(const mcs_desc* desc, const void* q_host,
     const void* rc = residual ? static_cast<const uint8_t*>(residual) + off : nullptr;
     st = sparse_impl(dc, residual ? mcs::kEpiAddResidual : mcs::kEpiPlain, slot_ptr(slot, 0), slot_ptr(slot, 1),
                      slot_ptr(slot, 2), perm + size_t(bh0) * dm.N_pad, idx + size_t(bh0) * dm.G * size_t(K), K, rc,
-                     slot_ptr(slot, 3), nullptr, status, s);
+                     slot_ptr(slot, 3), nullptr, status, cs[slot]);
     if (st != MCS_OK) break;
-    okc = cudaEventRecord(ev_done[slot], s) == cudaSuccess && cudaStreamWaitEvent(d2h, ev_done[slot], 0) == cudaSuccess &&
+    okc = cudaEventRecord(ev_done[slot], cs[slot]) == cudaSuccess &&
+          cudaStreamWaitEvent(d2h, ev_done[slot], 0) == cudaSuccess &&
           cudaMemcpyAsync(static_cast<uint8_t*>(o_host) + off, slot_ptr(slot, 3), bytes, cudaMemcpyDeviceToHost, d2h) ==
               cudaSuccess &&
           cudaEventRecord(ev_free[slot], d2h) == cudaSuccess;
   }
-  // the caller's stream completes after every copy
+  // the caller's stream completes after every copy (each copy-out follows its kernel)
   if (okc && st == MCS_OK)
     okc = cudaEventRecord(end, d2h) == cudaSuccess && cudaStreamWaitEvent(s, end, 0) == cudaSuccess;
   cleanup();
