@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--no-sweep", action="store_true", help="skip the 65,536-token density/tile sweep")
     ap.add_argument("--no-ring", action="store_true", help="skip the host-resident meta-cache (cache ring) timing")
     ap.add_argument("--no-matched", action="store_true", help="skip the PDDP-vs-contiguous group mass comparison")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the host-buffer end-to-end leg (profiler launch lists of the timed steps only)")
     ap.add_argument("--heads", type=int, default=None, help="override H (smaller case for profiler captures)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget (CPU seconds)")
     ap.add_argument("--e2e-chunks", type=int, default=40, help="head chunks of the host-buffer reuse step (one head each by default)")
@@ -429,28 +431,30 @@ def run_mcs(args, wl, K):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms, sparse_ms = float(t[0]), float(t[1])
 
-    # end to end through the C ABI from pinned host buffers: one call copies q, k, v in,
-    # runs the reuse step and copies o out, pipelined over head chunks
-    hq, hk, hv = (x.cpu().pin_memory() for x in (q2, k2, v2))
-    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    hws = mcs.host_gather_workspace(desc, args.e2e_chunks)
-    mcs.mcs_sparse_attn_gather_host(desc, hq, hk, hv, cache["perm"], cache["idx"], K, cache["residual"], ho, hws,
-                                    args.e2e_chunks, stream)
-    # per-call device times; the median rejects a call slowed by other traffic on the host link
-    e2e_calls = []
-    for _ in range(5):
-        torch.cuda.synchronize()
-        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ea.record(stream)
+    e2e_ms, e2e_calls = None, []
+    if not args.no_e2e:
+        # end to end through the C ABI from pinned host buffers: one call copies q, k, v in,
+        # runs the reuse step and copies o out, pipelined over head chunks
+        hq, hk, hv = (x.cpu().pin_memory() for x in (q2, k2, v2))
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        hws = mcs.host_gather_workspace(desc, args.e2e_chunks)
         mcs.mcs_sparse_attn_gather_host(desc, hq, hk, hv, cache["perm"], cache["idx"], K, cache["residual"], ho, hws,
                                         args.e2e_chunks, stream)
-        eb.record(stream)
-        torch.cuda.synchronize()
-        e2e_calls.append(ea.elapsed_time(eb))
-    mcs.mcs_check_status()
-    e2e_ms = statistics.median(e2e_calls)
-    del hws
-    if world > 1:
+        # per-call device times; the median rejects a call slowed by other traffic on the host link
+        e2e_calls = []
+        for _ in range(5):
+            torch.cuda.synchronize()
+            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ea.record(stream)
+            mcs.mcs_sparse_attn_gather_host(desc, hq, hk, hv, cache["perm"], cache["idx"], K, cache["residual"], ho, hws,
+                                            args.e2e_chunks, stream)
+            eb.record(stream)
+            torch.cuda.synchronize()
+            e2e_calls.append(ea.elapsed_time(eb))
+        mcs.mcs_check_status()
+        e2e_ms = statistics.median(e2e_calls)
+        del hws
+    if world > 1 and e2e_ms is not None:
         t = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t[0])
@@ -496,7 +500,8 @@ def run_mcs(args, wl, K):
             "fraction_of_ideal": dense_ms / sparse_ms * float(wl.density),
             "dense_tflops": flops_dense(wl) / (dense_ms * 1e-3) / 1e12,
             "gpu_launches": launches,
-            "e2e": {"value": e2e_ms / world, "unit": UNIT, "h2d_bytes_per_step": 3 * q2.numel() * q2.element_size(),
+            "e2e": None if e2e_ms is None else {
+                    "value": e2e_ms / world, "unit": UNIT, "h2d_bytes_per_step": 3 * q2.numel() * q2.element_size(),
                     "d2h_bytes_per_step": o.numel() * o.element_size(),
                     "api": f"mcs_sparse_attn_gather_host, pinned host q/k/v/o, {args.e2e_chunks} head chunks",
                     "calls_ms": [round(x, 3) for x in e2e_calls], "stat": "median of 5 calls"},
