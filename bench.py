@@ -68,6 +68,8 @@ def parse():
                     help="skip the host-buffer end-to-end leg (profiler launch lists of the timed steps only)")
     ap.add_argument("--heads", type=int, default=None, help="override H (smaller case for profiler captures)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget (CPU seconds)")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="--impl reference: total oracle budget over the warm-up and timed steps (CPU seconds)")
     ap.add_argument("--e2e-chunks", type=int, default=40, help="head chunks of the host-buffer reuse step (one head each by default)")
     return ap.parse_args()
 
@@ -77,6 +79,19 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def max_over_ranks(vals, device=None):
+    """Element-wise maximum of a list of floats over all ranks of the default
+    process group (NCCL on GPUs, gloo on CPUs); the values unchanged without one."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in vals]
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
 
 
 def peaks():
@@ -180,7 +195,7 @@ def run_reference(args, wl, K):
     if rank != 0:
         return
     per = []
-    budget = max(1.0, 60.0 / max(1, args.warmup + args.steps))
+    budget = max(0.5, args.ref_seconds / max(1, args.warmup + args.steps))
     for i in range(args.warmup + args.steps):
         dt, g, thr = oracle_sample(wl, K, budget, seed=i)
         if i >= args.warmup:
@@ -426,10 +441,7 @@ def run_mcs(args, wl, K):
     total_ms = t_start.elapsed_time(t_end)
     stage_ms = {s: [a.elapsed_time(b) for a, b in ev[s]] for s in stages}
     sparse_ms = statistics.mean(stage_ms["sparse"])
-    if world > 1:
-        t = torch.tensor([total_ms, sparse_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, sparse_ms = float(t[0]), float(t[1])
+    total_ms, sparse_ms = max_over_ranks([total_ms, sparse_ms], dev)
 
     e2e_ms, e2e_calls = None, []
     if not args.no_e2e:
@@ -454,10 +466,9 @@ def run_mcs(args, wl, K):
         mcs.mcs_check_status()
         e2e_ms = statistics.median(e2e_calls)
         del hws
-    if world > 1 and e2e_ms is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    if e2e_ms is not None:
+        e2e_ms = max_over_ranks([e2e_ms], dev)[0]
+    if world > 1:
         dist.barrier()
 
     if rank == 0:
