@@ -9,7 +9,10 @@ from sparse_attention_diffusion_gb300 import mcs, synth
 
 pytestmark = pytest.mark.gpu
 
-LAYERS = [synth.Workload("t", 1, 2, (3, 10, 20), 128, "bf16", 128, "0.2", seed=21 + l) for l in range(3)]
+CASES = {
+    "bf16-d128-c128": [synth.Workload("t", 1, 2, (3, 10, 20), 128, "bf16", 128, "0.2", seed=21 + l) for l in range(3)],
+    "f32-d64-c64": [synth.Workload("t", 1, 2, (4, 16, 16), 64, "f32", 64, "0.25", seed=31 + l) for l in range(3)],
+}
 
 
 def _anchor(desc, K, q, k, v, perm, idx, residual):
@@ -23,12 +26,12 @@ def _anchor(desc, K, q, k, v, perm, idx, residual):
     mcs.mcs_anchor_residual(desc, q, k, v, perm, idx, K, o_dense, residual)
 
 
-@pytest.fixture(scope="module")
-def layers():
+@pytest.fixture(scope="module", params=list(CASES))
+def layers(request):
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     mcs.load(build_if_missing=True)
     out = []
-    for wl in LAYERS:
+    for wl in CASES[request.param]:
         layer = synth.make_layer(wl)
         q, k, v = (t.cuda() for t in layer.cast())
         layer.drift_step()
@@ -39,14 +42,14 @@ def layers():
         _anchor(desc, K, q, k, v, cache["perm"], cache["idx"], cache["residual"])
         want = torch.empty_like(q2)
         mcs.mcs_sparse_attn_gather(desc, q2, k2, v2, cache["perm"], cache["idx"], K, cache["residual"], want)
-        out.append(dict(desc=desc, K=K, qkv=(q, k, v), qkv2=(q2, k2, v2), want=want))
+        out.append(dict(desc=desc, K=K, qkv=(q, k, v), qkv2=(q2, k2, v2), want=want, dtype=q.dtype))
     mcs.mcs_check_status()
     return out
 
 
 def test_ring_round_trip_matches_resident_caches(layers):
     desc, K = layers[0]["desc"], layers[0]["K"]
-    ring = mcs.CacheRing(desc, K, len(layers), torch.bfloat16)
+    ring = mcs.CacheRing(desc, K, len(layers), layers[0]["dtype"])
     try:
         for l, L in enumerate(layers):               # anchor step: fresh entries, stored to host
             c = ring.acquire(l, fill=False, prefetch_next=False)
@@ -70,7 +73,7 @@ def test_ring_round_trip_matches_resident_caches(layers):
 
 def test_ring_refuses_out_of_order_calls(layers):
     desc, K = layers[0]["desc"], layers[0]["K"]
-    ring = mcs.CacheRing(desc, K, 3, torch.bfloat16)
+    ring = mcs.CacheRing(desc, K, 3, layers[0]["dtype"])
     try:
         ring.acquire(0, fill=False, prefetch_next=False)
         with pytest.raises(mcs.McsError):
