@@ -30,6 +30,7 @@ struct TcColsumParams {
   float* scores;                // [nrows, N] fp32 rows of this launch
   int BH, N, N_pad, C, G;
   int row0;                     // first group row (bh * G + g) of this launch
+  int nrows;                    // group rows of this launch (set by tc_colsum)
   float scale_log2;
   uint32_t* status;
 };
