@@ -241,9 +241,16 @@ class CacheRing:
                                                                          _stream(stream)))
 
     def close(self):
+        """Wait for the ring's copies and free it (the buffers stay with this object)."""
         if self._ring:
             _check("mcs_cache_ring_destroy", load().mcs_cache_ring_destroy(self._ring))
             self._ring = ctypes.c_void_p()
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
 
 
 def mcs_anchor_residual(desc, q, k, v, perm, idx, K, o_dense, r, stream=None):

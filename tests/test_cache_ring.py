@@ -73,8 +73,7 @@ def test_ring_round_trip_matches_resident_caches(layers):
 
 def test_ring_refuses_out_of_order_calls(layers):
     desc, K = layers[0]["desc"], layers[0]["K"]
-    ring = mcs.CacheRing(desc, K, 3, layers[0]["dtype"])
-    try:
+    with mcs.CacheRing(desc, K, 3, layers[0]["dtype"]) as ring:
         ring.acquire(0, fill=False, prefetch_next=False)
         with pytest.raises(mcs.McsError):
             ring.acquire(0, fill=False)               # acquired twice
@@ -88,5 +87,3 @@ def test_ring_refuses_out_of_order_calls(layers):
         ring.acquire(2, fill=False, prefetch_next=False)
         ring.release(2)
         torch.cuda.synchronize()
-    finally:
-        ring.close()
