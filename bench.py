@@ -223,10 +223,10 @@ RING_LAYERS = 3
 def cache_ring_timing(desc, K, q, k, v, cache, stream):
     """Reuse steps whose meta-cache lives in pinned host memory: RING_LAYERS
     entries (copies of this layer's anchor cache, written out through the ring
-    as an anchor step would), then rounds over the layers where each layer's
+    as an anchor step would), then passes over the layers where each layer's
     entry is already resident from the previous layer's prefetch and the next
     one is copied in during its kernel. Returns ms per layer of the second
-    round (device events on the compute stream)."""
+    pass (device events on the compute stream)."""
     import torch
 
     from sparse_attention_diffusion_gb300 import mcs
@@ -238,7 +238,7 @@ def cache_ring_timing(desc, K, q, k, v, cache, stream):
             for key in ("perm", "idx", "residual"):
                 c[key].copy_(cache[key])
             ring.release(l, store=True, stream=stream)
-        per_round = []
+        per_pass = []
         for _ in range(2):
             torch.cuda.synchronize()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -249,11 +249,11 @@ def cache_ring_timing(desc, K, q, k, v, cache, stream):
                 ring.release(l, stream=stream)
             b.record(stream)
             torch.cuda.synchronize()
-            per_round.append(a.elapsed_time(b) / RING_LAYERS)
+            per_pass.append(a.elapsed_time(b) / RING_LAYERS)
         mcs.mcs_check_status()
-        return {"ms_per_layer": per_round[-1], "first_round_ms_per_layer": per_round[0],
+        return {"ms_per_layer": per_pass[-1], "first_pass_ms_per_layer": per_pass[0],
                 "entry_bytes": ring.entry, "layers": RING_LAYERS,
-                "note": "perm+idx+residual per layer in pinned host memory, two device slots; round 2 timed"}
+                "note": "perm+idx+residual per layer in pinned host memory, two device slots; second pass over the layers timed"}
     finally:
         ring.close()
 

@@ -66,7 +66,7 @@ def test_ring_round_trip_matches_resident_caches(layers):
             torch.cuda.synchronize()
             mcs.mcs_check_status()
             for l, (o, L) in enumerate(zip(outs, layers)):
-                assert torch.equal(o, L["want"]), f"round {rnd} layer {l}: ring cache differs from resident cache"
+                assert torch.equal(o, L["want"]), f"pass {rnd} layer {l}: ring cache differs from resident cache"
     finally:
         ring.close()
 
