@@ -1,7 +1,8 @@
 """bf16 layers small enough for the oracle, spanning several tiles with ragged
 tails (N not a multiple of 128, K not a multiple of 128, pad queries, K = N),
-both head dims and both group sizes. Every stage of the CUDA path is checked
-against the float64 oracle run on the very tensors the GPU received."""
+both head dims and both group sizes, and a layer of one group per head. Every
+stage of the CUDA path is checked against the float64 oracle run on the very
+tensors the GPU received."""
 import numpy as np
 import pytest
 import torch
@@ -20,6 +21,8 @@ CASES = {
     "n600-d64-c128-k150": synth.Workload("t", 1, 1, (3, 10, 20), 64, "bf16", 128, "0.25", seed=7),
     "n1024-d128-c128-k205": synth.Workload("t", 2, 1, (2, 16, 32), 128, "bf16", 128, "0.2", seed=8),
     "n600-d128-c128-kN": synth.Workload("t", 1, 1, (3, 10, 20), 128, "bf16", 128, "1.0", seed=9),
+    # one group per head (G = 1, 28 pad rows): no split at all, a key list shorter than one tile
+    "n100-d128-c128-k30": synth.Workload("t", 1, 2, (1, 10, 10), 128, "bf16", 128, "0.3", seed=10),
 }
 
 
