@@ -1,9 +1,11 @@
-"""The 720p kernel-benchmark layer at full size, in the launch configuration the
-benchmark times (B=1, H=40, N=75,600 on a 21x45x80 grid, d=128, bf16, C=128,
-K=15,120): the whole path runs on the GPU (grouping, dense attention + LSE,
+"""Full-size layers in the launch configuration the benchmark uses: the 720p
+kernel-benchmark layer (B=1, H=40, N=75,600 on a 21x45x80 grid, d=128, bf16,
+C=128, K=15,120), the Wan2.1-1.3B-shaped 480p layer (H=12, N=32,768, K=6,554)
+and the 118,800-token schedule layer (H=24, 929 groups with 112 pad rows,
+K=17,820). The whole path runs on the GPU (grouping, dense attention + LSE,
 pass-2 selection, anchor residual, one drifted reuse step), and sampled heads,
 groups and rows are checked one by one against the float64 oracle fed the very
-tensors the GPU received (the oracle cannot run the whole layer in a test)."""
+tensors the GPU received (the oracle cannot run a whole layer in a test)."""
 import numpy as np
 import pytest
 import torch
@@ -14,16 +16,21 @@ from tests import parity
 
 pytestmark = pytest.mark.gpu
 
-HEADS = (0, 17, 39)        # sampled heads
 GROUPS_PER_HEAD = 2        # sampled groups per head (selection, residual, reuse)
 ROWS_PER_HEAD = 64         # sampled query rows per head (dense output and LSE)
+LAYERS = {
+    "kernel-bench-720p": synth.KBENCH_720P,
+    "wan2.1-1.3b-480p": synth.WAN13_480P,
+    "schedule-118800": synth.SCHEDULE_HY,
+}
 
 
-@pytest.fixture(scope="module")
-def run():
+@pytest.fixture(scope="module", params=list(LAYERS))
+def run(request):
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     mcs.load(build_if_missing=True)
-    wl = synth.KBENCH_720P
+    wl = LAYERS[request.param]
+    heads = (0, wl.H // 2 - 3, wl.H - 1)   # first, middle, last
     layer = synth.make_layer(wl, device="cuda")
     q, k, v = layer.cast()
     desc = mcs.desc_for(q, wl.C)
@@ -45,15 +52,19 @@ def run():
     host = lambda t, h: parity.f64(t[0, h])
     out = dict(wl=wl, K=K, heads={})
     rng = np.random.default_rng(20261202)
-    for h in HEADS:
+    for h in heads:
+        groups = rng.choice(wl.G, GROUPS_PER_HEAD, replace=False)
+        if wl.N_pad > wl.N:
+            groups[-1] = wl.G - 1          # the group that holds the pad rows
         out["heads"][h] = dict(
             q=host(q, h), k=host(k, h), v=host(v, h), q2=host(q2, h), k2=host(k2, h), v2=host(v2, h),
             o_dense=host(o_dense, h), lse=lse[0, h].double().cpu().numpy(), o_reuse=host(o_reuse, h),
             residual=host(cache["residual"], h), perm=cache["perm"][0, h].cpu().numpy(),
             group_of=cache["group_of"][0, h].cpu().numpy(), idx=cache["idx"][0, h].cpu().numpy(),
             mass=cache["mass"][0, h].cpu().numpy(),
-            rows=rng.choice(wl.N, ROWS_PER_HEAD, replace=False),
-            groups=rng.choice(wl.G, GROUPS_PER_HEAD, replace=False))
+            rows=rng.choice(wl.N, ROWS_PER_HEAD, replace=False), groups=groups)
+    del q, k, v, q2, k2, v2, o_dense, lse, o_reuse, cache, ws, layer
+    torch.cuda.empty_cache()
     return out
 
 
