@@ -34,7 +34,10 @@
  *     index out of range) do not stop the kernel: the offending row is skipped,
  *     a sticky flag is raised, and mcs_check_status() reports it.
  *   - The library allocates no device memory except one small static word of
- *     device status flags; all scratch space is the caller's workspace.
+ *     device status flags and the fixed 64 MiB static score array of
+ *     mcs_anchor_select_noalloc; all other scratch space is the caller's
+ *     workspace. (mcs_sparse_attn_gather_host and the meta-cache ring create
+ *     CUDA streams and events, no memory.)
  *   - No C++ exception crosses this boundary.
  */
 #ifndef MCS_H_
