@@ -143,17 +143,43 @@ def workspace(desc: mcs_desc, K: int = 1, device="cuda") -> torch.Tensor:
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
+def _io_dtype(desc):
+    return torch.bfloat16 if desc.dtype == MCS_BF16 else torch.float32
+
+
+def _expect(desc, K=None, **tensors):
+    """Host check of tensors against the descriptor before their pointers cross
+    the ABI (the library trusts the descriptor's sizes): x-like tensors are
+    [B,H,N,d] in the I/O dtype, perm [B,H,N_pad] int32, group_of [B,H,N] int32,
+    lse [B,H,N] fp32, idx [B,H,G,K] int32, mass [B,H,G] fp32. None is allowed."""
+    G, N_pad = geometry(desc)
+    B, H, N, d = desc.B, desc.H, desc.N, desc.d
+    want = {"x": ((B, H, N, d), _io_dtype(desc)), "perm": ((B, H, N_pad), torch.int32),
+            "group_of": ((B, H, N), torch.int32), "lse": ((B, H, N), torch.float32),
+            "idx": ((B, H, G, K), torch.int32), "mass": ((B, H, G), torch.float32)}
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        kind = name if name in want else "x"
+        shape, dtype = want[kind]
+        if tuple(t.shape) != tuple(shape) or t.dtype != dtype:
+            raise ValueError(f"{name}: expected {tuple(shape)} {dtype}, got {tuple(t.shape)} {t.dtype}")
+
+
 def mcs_group_pddp(desc, q, perm, group_of, ws, stream=None):
+    _expect(desc, q=q, perm=perm, group_of=group_of)
     _check("mcs_group_pddp", load().mcs_group_pddp(ctypes.byref(desc), _ptr(q), _ptr(perm), _ptr(group_of), _ptr(ws),
                                                    ws.numel(), _stream(stream)))
 
 
 def mcs_dense_attn(desc, q, k, v, o, lse, stream=None):
+    _expect(desc, q=q, k=k, v=v, o=o, lse=lse)
     _check("mcs_dense_attn", load().mcs_dense_attn(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                                    _stream(stream)))
 
 
 def mcs_anchor_select(desc, q, k, perm, lse, K, idx, mass, ws, stream=None):
+    _expect(desc, int(K), q=q, k=k, perm=perm, lse=lse, idx=idx, mass=mass)
     _check("mcs_anchor_select", load().mcs_anchor_select(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(perm), _ptr(lse),
                                                          int(K), _ptr(idx), _ptr(mass), _ptr(ws), ws.numel(),
                                                          _stream(stream)))
@@ -161,12 +187,14 @@ def mcs_anchor_select(desc, q, k, perm, lse, K, idx, mass, ws, stream=None):
 
 def mcs_anchor_select_noalloc(desc, q, k, perm, lse, K, idx, mass, stream=None):
     """mcs_anchor_select without a workspace (scores kept in the library's fixed device array)."""
+    _expect(desc, int(K), q=q, k=k, perm=perm, lse=lse, idx=idx, mass=mass)
     _check("mcs_anchor_select_noalloc", load().mcs_anchor_select_noalloc(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(perm),
                                                                          _ptr(lse), int(K), _ptr(idx), _ptr(mass),
                                                                          _stream(stream)))
 
 
 def mcs_sparse_attn_gather(desc, q, k, v, perm, idx, K, residual, o, stream=None):
+    _expect(desc, int(K), q=q, k=k, v=v, perm=perm, idx=idx, residual=residual, o=o)
     _check("mcs_sparse_attn_gather", load().mcs_sparse_attn_gather(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v),
                                                                    _ptr(perm), _ptr(idx), int(K), _ptr(residual),
                                                                    _ptr(o), _stream(stream)))
@@ -190,6 +218,7 @@ def host_gather_workspace(desc, head_chunks, device="cuda") -> torch.Tensor:
 def mcs_sparse_attn_gather_host(desc, q_host, k_host, v_host, perm, idx, K, residual, o_host, ws, head_chunks,
                                 stream=None):
     """Reuse-step sparse attention from host q/k/v (pinned for overlap) to a host output."""
+    _expect(desc, int(K), q=q_host, k=k_host, v=v_host, perm=perm, idx=idx, residual=residual, o=o_host)
     _check("mcs_sparse_attn_gather_host", load().mcs_sparse_attn_gather_host(
         ctypes.byref(desc), _host_ptr(q_host), _host_ptr(k_host), _host_ptr(v_host), _ptr(perm), _ptr(idx), int(K),
         _ptr(residual), _host_ptr(o_host), _ptr(ws), ws.numel() * ws.element_size(), int(head_chunks),
@@ -254,17 +283,20 @@ class CacheRing:
 
 
 def mcs_anchor_residual(desc, q, k, v, perm, idx, K, o_dense, r, stream=None):
+    _expect(desc, int(K), q=q, k=k, v=v, perm=perm, idx=idx, o_dense=o_dense, r=r)
     _check("mcs_anchor_residual", load().mcs_anchor_residual(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(perm),
                                                              _ptr(idx), int(K), _ptr(o_dense), _ptr(r),
                                                              _stream(stream)))
 
 
 def mcs_residual_store(desc, o_dense, o_sparse, r, stream=None):
+    _expect(desc, o_dense=o_dense, o_sparse=o_sparse, r=r)
     _check("mcs_residual_store", load().mcs_residual_store(ctypes.byref(desc), _ptr(o_dense), _ptr(o_sparse), _ptr(r),
                                                            _stream(stream)))
 
 
 def mcs_residual_apply(desc, o_sparse, r, o, stream=None):
+    _expect(desc, o_sparse=o_sparse, r=r, o=o)
     _check("mcs_residual_apply", load().mcs_residual_apply(ctypes.byref(desc), _ptr(o_sparse), _ptr(r), _ptr(o),
                                                            _stream(stream)))
 

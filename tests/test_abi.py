@@ -127,3 +127,20 @@ def test_cache_ring_validation(lib):
     assert lib.mcs_cache_ring_acquire(None, 0, 1, 1, None, ctypes.byref(p), ctypes.byref(p), ctypes.byref(p)) == 1
     assert lib.mcs_cache_ring_release(None, 0, 0, None) == 1
     assert lib.mcs_cache_ring_destroy(None) == 1
+
+
+def test_binding_checks_shapes_against_the_descriptor():
+    import torch
+
+    d = _desc()                                   # B=1, H=2, N=600 (N_pad 640, G 5), d=128, bf16
+    ok = dict(q=torch.empty(1, 2, 600, 128, dtype=torch.bfloat16), perm=torch.empty(1, 2, 640, dtype=torch.int32),
+              idx=torch.empty(1, 2, 5, 120, dtype=torch.int32), lse=torch.empty(1, 2, 600))
+    mcs._expect(d, 120, **ok)
+    for name, bad in [("q", torch.empty(1, 2, 600, 64, dtype=torch.bfloat16)),
+                      ("q", torch.empty(1, 2, 600, 128, dtype=torch.float32)),
+                      ("perm", torch.empty(1, 2, 600, dtype=torch.int32)),
+                      ("idx", torch.empty(1, 2, 5, 121, dtype=torch.int32)),
+                      ("lse", torch.empty(1, 2, 600, dtype=torch.float64))]:
+        with pytest.raises(ValueError):
+            mcs._expect(d, 120, **dict(ok, **{name: bad}))
+    mcs._expect(d, 120, lse=None, mass=None)      # optional outputs may be absent
