@@ -57,6 +57,22 @@ def test_host_gather_matches_device_gather(prepared, chunks, with_residual):
     assert torch.equal(ho, want.cpu()), "host-buffer reuse step differs from the device-buffer one"
 
 
+def test_host_gather_from_pageable_memory(prepared):
+    """Pageable host buffers are correct too (the copies then serialise)."""
+    desc, K, cache = prepared["desc"], prepared["K"], prepared["cache"]
+    hq, hk, hv = (t.clone() for t in prepared["host"])          # plain (pageable) host copies
+    assert not hq.is_pinned()
+    dq, dk, dv = (t.cuda() for t in (hq, hk, hv))
+    want = torch.empty_like(dq)
+    mcs.mcs_sparse_attn_gather(desc, dq, dk, dv, cache["perm"], cache["idx"], K, cache["residual"], want)
+    ho = torch.empty(hq.shape, dtype=hq.dtype)
+    ws = mcs.host_gather_workspace(desc, 2)
+    mcs.mcs_sparse_attn_gather_host(desc, hq, hk, hv, cache["perm"], cache["idx"], K, cache["residual"], ho, ws, 2)
+    torch.cuda.current_stream().synchronize()
+    mcs.mcs_check_status()
+    assert torch.equal(ho, want.cpu())
+
+
 def test_host_gather_repeated_calls_on_one_stream(prepared):
     """Back-to-back calls reuse one workspace: each call's copy-in waits for the
     previous call's kernels and copy-out through the caller's stream."""
