@@ -19,7 +19,9 @@
 //                                 (through perm) once, then per tile the key
 //                                 and value rows at the group's index list, as
 //                                 16-byte cp.async copies into 3-stage K and V
-//                                 rings (128-byte swizzled);
+//                                 rings (128-byte swizzled); eight threads per
+//                                 row, each copying one chunk of every 128-byte
+//                                 half, so a thread holds 4 row ids per tile;
 //   warpgroup 4 (warp 16)         tensor-memory allocation and the MMA
 //                                 schedule, run by the whole warp with lane 0
 //                                 issuing (warps 17-19 idle).
@@ -76,9 +78,13 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
   using L = SparseCfg<D>;
   constexpr int SK = L::kSK, SV = L::kSV;
   static_assert(SK == SV, "one stage index for tile i's key and value rows");
-  constexpr int kChunks = D / 8;  // 16-byte chunks per row
-  constexpr int kRowsPerPass = kGather / kChunks;
-  constexpr int kPasses = 128 / kRowsPerPass;
+  // gather mapping: a thread copies 16-byte chunk ch of the row's first 64
+  // elements and chunk ch of the next 64 (d = 128: two 128-byte halves, each
+  // copy instruction reading whole 128-byte segments), 8 threads per row
+  constexpr int kChunks = 8;
+  constexpr int kHalves = D / 64;
+  constexpr int kRowsPerPass = kGather / kChunks;  // 32
+  constexpr int kPasses = 128 / kRowsPerPass;      // 4 ids per thread per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -190,7 +196,10 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
           if (v < 0 || v >= p.N_pad) raise_status(st, kStatusBounds);
           else if (v < p.N) tq = v;
         }
-        cp_async16(sbase + L::kQ + sw128_off(row, ch), qb + size_t(tq < 0 ? 0 : tq) * D + ch * 8, tq >= 0);
+#pragma unroll
+        for (int h = 0; h < kHalves; ++h)
+          cp_async16(sbase + L::kQ + h * kRegion + sw128_off(row, ch), qb + size_t(tq < 0 ? 0 : tq) * D + h * 64 + ch * 8,
+                     tq >= 0);
       }
       cp_async_arrive_noinc(q_full);
     }
@@ -230,11 +239,15 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
       if (all_valid) {
 #pragma unroll
         for (int it = 0; it < kPasses; ++it)
-          cp_async16(dk + it * kRowsPerPass * 128, kbc + size_t(uint32_t(ids[it])) * D, true);
+#pragma unroll
+          for (int h = 0; h < kHalves; ++h)
+            cp_async16(dk + h * kRegion + it * kRowsPerPass * 128, kbc + size_t(uint32_t(ids[it])) * D + h * 64, true);
         cp_async_arrive_noinc(k_full + s);
 #pragma unroll
         for (int it = 0; it < kPasses; ++it)
-          cp_async16(dv + it * kRowsPerPass * 128, vbc + size_t(uint32_t(ids[it])) * D, true);
+#pragma unroll
+          for (int h = 0; h < kHalves; ++h)
+            cp_async16(dv + h * kRegion + it * kRowsPerPass * 128, vbc + size_t(uint32_t(ids[it])) * D + h * 64, true);
         cp_async_arrive_noinc(v_full + s);
       } else {
 #pragma unroll
@@ -247,11 +260,17 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
         }
 #pragma unroll
         for (int it = 0; it < kPasses; ++it)
-          cp_async16(dk + it * kRowsPerPass * 128, kbc + size_t(ids[it] < 0 ? 0 : ids[it]) * D, ids[it] >= 0);
+#pragma unroll
+          for (int h = 0; h < kHalves; ++h)
+            cp_async16(dk + h * kRegion + it * kRowsPerPass * 128, kbc + size_t(ids[it] < 0 ? 0 : ids[it]) * D + h * 64,
+                       ids[it] >= 0);
         cp_async_arrive_noinc(k_full + s);
 #pragma unroll
         for (int it = 0; it < kPasses; ++it)
-          cp_async16(dv + it * kRowsPerPass * 128, vbc + size_t(ids[it] < 0 ? 0 : ids[it]) * D, ids[it] >= 0);
+#pragma unroll
+          for (int h = 0; h < kHalves; ++h)
+            cp_async16(dv + h * kRegion + it * kRowsPerPass * 128, vbc + size_t(ids[it] < 0 ? 0 : ids[it]) * D + h * 64,
+                       ids[it] >= 0);
         cp_async_arrive_noinc(v_full + s);
       }
       return true;
