@@ -46,9 +46,9 @@ UNIT = "ms/layer"
 REUSE_PER_STEP = 9
 # DRAM bytes (read + write) of one reuse-kernel launch on the 40-head layer: an
 # 8-head ncu capture scaled by heads (traffic grows in proportion); the summary is
-# profiles/attn_sparse_kernel-kernel-bench-720p-h8.md (1.0790 GB read + 0.1584 GB
+# profiles/attn_sparse_kernel-kernel-bench-720p-h8.md (1.0941 GB read + 0.1487 GB
 # written per 8-head launch). Set to None when the kernel changes.
-SPARSE_TRAFFIC_BYTES_H40 = (1.0790e9 + 0.1584e9) * 40 / 8
+SPARSE_TRAFFIC_BYTES_H40 = (1.0941e9 + 0.1487e9) * 40 / 8
 
 
 def parse():
