@@ -122,6 +122,58 @@ def test_pddp_line_clusters_in_order():
         assert len(set((perm[g * C:(g + 1) * C] // C).tolist())) == 1
 
 
+def _golden_kv(name):
+    """Parse a `key | values` golden file; lines under `points` are `id | x | y`."""
+    kv, pts = {}, []
+    in_points = False
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            if line.strip() == "points":
+                in_points = True
+                continue
+            parts = [t.strip() for t in line.split("|")]
+            if in_points and len(parts) == 3 and parts[0].lstrip("-").isdigit():
+                pts.append((int(parts[0]), float(parts[1]), float(parts[2])))
+                continue
+            in_points = False
+            kv[parts[0]] = parts[1]
+    return kv, pts
+
+
+def test_pddp_hand_worked_odd_split():
+    """G = 3: the root sends floor(3/2) = 1 group left, and the right node's own
+    principal direction (not the root's) cuts the remaining points. Hand-worked in
+    tests/golden/pddp_odd_split.txt; a ceil(n/2) split gives different groups."""
+    kv, pts = _golden_kv("pddp_odd_split.txt")
+    C = int(kv["C"])
+    x = np.zeros((len(pts), 2))
+    for i, a, b in pts:
+        x[i] = (a, b)
+    perm, group_of = orc.pddp_groups(x, len(pts), C, iters=20)
+    assert perm.tolist() == [int(t) for t in kv["perm"].split()]
+    assert group_of.tolist() == [int(t) for t in kv["group_of"].split()]
+
+
+def test_pddp_hand_worked_pads_excluded():
+    """Pads (zero rows at ids >= N) enter neither the node mean nor its covariance:
+    with them, the x axis would win and a different real token would share the pad
+    group. Hand-worked in tests/golden/pddp_pads.txt."""
+    kv, _ = _golden_kv("pddp_pads.txt")
+    N, C = int(kv["N"]), int(kv["C"])
+    i = np.arange(N)
+    y = (37 * i % 65) - 32.0
+    x = np.zeros((2 * C, 2))
+    x[:N, 0] = 100.0 + 0.001 * (352.0 - y * y)
+    x[:N, 1] = y
+    perm, group_of = orc.pddp_groups(x, N, C, iters=20)
+    want1 = [int(t) for t in kv["group1"].split()]
+    assert perm[C:].tolist() == want1
+    assert perm[:C].tolist() == [t for t in range(N) if t not in want1]
+    assert np.all(group_of[want1[:1]] == 1) and int((group_of == 0).sum()) == N - 1
+
+
 # ---------------------------------------------------------------- dense attention
 @pytest.mark.parametrize("N,Nk,d", [(37, 53, 16), (300, 300, 64), (5, 1, 8)])
 def test_dense_matches_sdpa_and_logsumexp(N, Nk, d):
