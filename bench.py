@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--no-sweep", action="store_true", help="skip the 65,536-token density/tile sweep")
     ap.add_argument("--no-ring", action="store_true", help="skip the host-resident meta-cache (cache ring) timing")
     ap.add_argument("--no-matched", action="store_true", help="skip the PDDP-vs-contiguous group mass comparison")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the tiny fp32 layer and the 480p-shaped layer (1 anchor + reuse steps each)")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer end-to-end leg (profiler launch lists of the timed steps only)")
     ap.add_argument("--heads", type=int, default=None, help="override H (smaller case for profiler captures)")
@@ -98,9 +100,10 @@ def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             j = json.load(f)
-        return dict(hbm=j["hbm_gbs"], bf16=j["bf16_tflops"], bf16_sus=j["bf16_tflops_sustained"], src="measured")
+        return dict(hbm=j["hbm_gbs"], bf16=j["bf16_tflops"], bf16_sus=j["bf16_tflops_sustained"],
+                    sm_max_mhz=float(j.get("sm_max_mhz", 2070.0)), src="measured")
     except Exception:
-        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, sm_max_mhz=2070.0, src="fallback")
 
 
 class Clocks:
@@ -188,6 +191,60 @@ def oracle_sample(wl, K, budget_s, seed=0):
     except Exception:
         threads = os.cpu_count() or threads
     return dt, n_groups, threads
+
+
+def oracle_anchor_sample(wl, K, n_groups=8, seed=0):
+    """Time the float64 oracle's anchor step on one head of the layer: the full
+    PDDP grouping, then for `n_groups` seeded groups of it the dense rows and
+    their LSE, the group scores, the top-K, the sparse rows and the residual, and
+    the reuse step (sparse rows + residual) of the same groups. Returns seconds
+    for the grouping of one head, per anchor group and per reuse group, and the
+    threads used; the caller extrapolates to the layer."""
+    import numpy as np
+    import torch
+    from oracle import mcs_oracle as orc
+    from sparse_attention_diffusion_gb300 import synth
+
+    one = wl.with_(B=1, H=1)
+    layer = synth.make_layer(one, device="cpu", seed=seed)
+    q, k, v = (t[0, 0].float().numpy().astype(np.float64) for t in layer.cast())
+    N, C = wl.N, wl.C
+    x = np.zeros((wl.N_pad, wl.d))
+    x[:N] = q
+    t0 = time.perf_counter()
+    perm, _ = orc.pddp_groups(x, N, C, 20)
+    t_pddp = time.perf_counter() - t0
+    rng = np.random.default_rng(seed)
+    groups = rng.choice(wl.G, min(n_groups, wl.G), replace=False)
+    t_anchor = t_reuse = 0.0
+    for g in groups:
+        mem = perm[g * C:(g + 1) * C]
+        mem = mem[mem < N]
+        t1 = time.perf_counter()
+        o_d, lse = orc.dense_attention(q[mem], k, v)
+        S = orc.group_scores(q[mem], lse, k)
+        idx = orc.topk_ascending(S, K)
+        r = o_d - orc.sparse_attention(q[mem], k, v, idx)
+        t2 = time.perf_counter()
+        _ = orc.sparse_attention(q[mem], k, v, idx) + r
+        t3 = time.perf_counter()
+        t_anchor += t2 - t1
+        t_reuse += t3 - t2
+    threads = torch.get_num_threads()
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max(int(i.get("num_threads", 1)) for i in threadpool_info()) or threads
+    except Exception:
+        threads = os.cpu_count() or threads
+    return dict(pddp_s=t_pddp, anchor_group_s=t_anchor / len(groups), reuse_group_s=t_reuse / len(groups),
+                groups=len(groups), threads=threads)
+
+
+def oracle_layer_ms(wl, smp):
+    """Per-layer extrapolation of an oracle_anchor_sample: anchor and reuse ms."""
+    BH = wl.B * wl.H
+    return dict(anchor=(smp["pddp_s"] * BH + smp["anchor_group_s"] * BH * wl.G) * 1e3,
+                reuse=smp["reuse_group_s"] * BH * wl.G * 1e3)
 
 
 def run_reference(args, wl, K):
@@ -285,7 +342,7 @@ def matched_density(desc, K, q, k, v, o_dense, cache, ws):
     return out
 
 
-def schedule_overhead(dev):
+def schedule_overhead(dev, peak_tflops):
     """The full meta-cache schedule on the 118,800-token layer (24 heads, 50 steps:
     5 dense warm-up steps, an anchor every 10 steps, reuse steps otherwise, drift
     0.05) at densities 0.15 and 0.25: total time including anchors and the anchor
@@ -308,10 +365,21 @@ def schedule_overhead(dev):
         t_dense = statistics.median(r.ms for r in recs[1:5])  # the first dense step pays one-off costs
         rho_eq, extra = schedule.anchor_overhead(recs, t_dense, float(wl.density), 5)
         kinds = {k: [r.ms for r in recs if r.kind == k] for k in ("dense", "anchor", "reuse")}
+        n_post = len(recs) - 5
+        n_anchor, n_reuse = len(kinds["anchor"]), len(kinds["reuse"])
+        t_reuse = statistics.mean(kinds["reuse"])
+        reuse_tf = flops_sparse(wl, wl.K) / (t_reuse * 1e-3) / 1e12
         out[rho] = {"K": wl.K, "total_ms": sum(r.ms for r in recs), "post_warmup_ms": sum(r.ms for r in recs[5:]),
                     "dense_step_ms": t_dense, "anchor_step_ms": statistics.mean(kinds["anchor"]),
-                    "reuse_step_ms": statistics.mean(kinds["reuse"]), "rho_eq": rho_eq,
-                    "anchor_overhead_points": 100.0 * extra,
+                    "anchor_stages_ms": {n: statistics.mean(r.stages[n] for r in recs if r.kind == "anchor")
+                                         for n in ("pddp", "dense", "select", "anchor_residual")},
+                    "reuse_step_ms": t_reuse, "reuse_tflops": reuse_tf, "reuse_frac": reuse_tf / peak_tflops,
+                    "rho_eq": rho_eq, "anchor_overhead_points": 100.0 * extra,
+                    # what an anchor that only ran dense attention would cost, with reuse at 1/rho of dense
+                    "floor_points_dense_anchor_ideal_reuse": 100.0 * n_anchor * (1.0 - float(rho)) / n_post,
+                    # the same with the measured reuse steps
+                    "floor_points_dense_anchor_measured_reuse":
+                        100.0 * ((n_anchor * t_dense + n_reuse * t_reuse) / (n_post * t_dense) - float(rho)),
                     "vs_all_dense": 50 * t_dense / sum(r.ms for r in recs)}
         del ml, layer, recs
         torch.cuda.empty_cache()
@@ -367,8 +435,114 @@ def sweep_table(dev, peak_tflops):
         mcs.mcs_check_status()
         del q, k, v, o_dense, lse, o, cache, ws
         torch.cuda.empty_cache()
+    table = {}
+    for r in rows:
+        t = table.setdefault(f"d{r['d']}-c{r['C']}", {"density": [], "K": [], "sparse_ms": [], "tflops": [],
+                                                       "frac": [], "speedup_vs_dense": [],
+                                                       "dense_ms": r["dense_ms"]})
+        for key in ("density", "K", "sparse_ms", "tflops", "frac", "speedup_vs_dense"):
+            t[key].append(_r(r[key]))
     return {"workload": synth.SWEEP.name, "B": 1, "H": synth.SWEEP.H, "N": synth.SWEEP.N,
-            "peak_kind": "measured sustained bf16", "rows": rows}
+            "peak_kind": "measured sustained bf16", "by_shape": table}
+
+
+def fp32_alu_peak_tflops(sm_max_mhz):
+    """FP32 FMA peak of the CUDA cores: SMs x 128 fp32 lanes x 2 FLOP x max SM clock."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return sms * 128 * 2 * sm_max_mhz * 1e6 / 1e12
+
+
+def config_measure(wl, dev, pk, n_reuse, cpu=True, reps=3, warm=2):
+    """One anchor step and `n_reuse` drifted reuse steps of a layer, repeated
+    (warm untimed + reps timed): per-stage ms (CUDA events, median), the reuse
+    kernel's kept TFLOP/s and roofline fraction, its speedup over the dense
+    kernel, and the float64 oracle on the host cores (the whole layer when it has
+    one head of at most 4,096 tokens, else one head's grouping and 8 sampled
+    groups, extrapolated)."""
+    import torch
+
+    from sparse_attention_diffusion_gb300 import mcs, schedule, synth
+
+    layer = synth.make_layer(wl, device=dev)
+    steps = [layer.cast()]
+    for _ in range(n_reuse):
+        layer.drift_step()
+        steps.append(layer.cast())
+    del layer
+    q, k, v = steps[0]
+    desc = mcs.desc_for(q, wl.C)
+    K = wl.K
+    ml = schedule.MetaCacheLayer(desc, K, q.dtype, dev)
+    stream = torch.cuda.current_stream()
+    ev = {n: [] for n in ("pddp", "dense", "select", "anchor_residual", "sparse")}
+
+    def timer(name, fn, keep=True):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        if keep:
+            ev[name].append((a, b))
+
+    for rep in range(warm + reps):
+        keep = rep >= warm
+        ml.anchor(q, k, v, lambda n, fn: timer(n, fn, keep))
+        for (q2, k2, v2) in steps[1:]:
+            timer("sparse", lambda: ml.reuse(q2, k2, v2), keep)
+    torch.cuda.synchronize()
+    mcs.mcs_check_status()
+    ms = {n: statistics.median(a.elapsed_time(b) for a, b in v) for n, v in ev.items()}
+    bf16 = wl.dtype == "bf16"
+    peak = pk["bf16_sus"] if bf16 else fp32_alu_peak_tflops(pk.get("sm_max_mhz", 2070.0))
+    tf = flops_sparse(wl, K) / (ms["sparse"] * 1e-3) / 1e12
+    out = {"workload": wl.name, "H": wl.H, "N": wl.N, "d": wl.d, "C": wl.C, "dtype": wl.dtype, "K": K,
+           "steps": f"1 anchor + {n_reuse} reuse", "stages_ms": ms,
+           "anchor_ms": sum(ms[n] for n in ("pddp", "dense", "select", "anchor_residual")),
+           "sparse_tflops": tf, "frac": tf / peak,
+           "peak": {"value": peak, "kind": f"{pk['src']} sustained bf16" if bf16 else
+                    "fp32 FMA lanes x 2 x max SM clock (derived)"},
+           "dense_tflops": flops_dense(wl) / (ms["dense"] * 1e-3) / 1e12,
+           "speedup_vs_dense": ms["dense"] / ms["sparse"], "ideal_speedup": 1.0 / float(wl.density)}
+    del ml, steps, q, k, v
+    torch.cuda.empty_cache()
+    if cpu:
+        out["cpu_baseline"] = oracle_config(wl, K)
+    return out
+
+
+def oracle_config(wl, K):
+    """The float64 oracle on the host cores for a config line: the whole layer
+    (anchor_head + reuse_head) for one head of <= 4,096 tokens, else one head's
+    grouping plus 8 sampled groups extrapolated to the layer."""
+    import numpy as np
+    import torch
+    from oracle import mcs_oracle as orc
+    from sparse_attention_diffusion_gb300 import synth
+
+    if wl.B * wl.H == 1 and wl.N <= 4096:
+        layer = synth.make_layer(wl, device="cpu")
+        q, k, v = (t[0, 0].float().numpy().astype(np.float64) for t in layer.cast())
+        t0 = time.perf_counter()
+        ref = orc.anchor_head(q, k, v, wl.C, K)
+        t1 = time.perf_counter()
+        orc.reuse_head(q, k, v, ref["perm"], ref["idx"], ref["residual"], wl.C)
+        t2 = time.perf_counter()
+        return {"anchor_ms": (t1 - t0) * 1e3, "reuse_ms": (t2 - t1) * 1e3, "cores": torch.get_num_threads(),
+                "kind": "oracle", "sample": "whole layer (one head), float64 numpy"}
+    smp = oracle_anchor_sample(wl, K)
+    ext = oracle_layer_ms(wl, smp)
+    return {"anchor_ms": ext["anchor"], "reuse_ms": ext["reuse"], "cores": smp["threads"], "kind": "oracle",
+            "sample": f"one head: full grouping ({smp['pddp_s']:.1f} s) + {smp['groups']} sampled groups "
+                      f"(dense rows, LSE, scores, top-K, sparse, residual; reuse), float64 numpy, "
+                      f"extrapolated to {wl.B * wl.H} heads x {wl.G} groups"}
+
+
+def _r(x, n=4):
+    """Round to n significant digits (compact summary)."""
+    if x is None or not isinstance(x, (int, float)) or x == 0 or not math.isfinite(x):
+        return x
+    return round(x, -int(math.floor(math.log10(abs(x)))) + n - 1)
 
 
 def run_mcs(args, wl, K):
@@ -525,9 +699,12 @@ def run_mcs(args, wl, K):
             ring["resident_ms_per_layer"] = sparse_ms
             line["cache_ring"] = ring
         if world == 1 and not args.no_schedule:
-            line["anchor_overhead"] = schedule_overhead(dev)
+            line["anchor_overhead"] = schedule_overhead(dev, pk["bf16_sus"])
         if world == 1 and not args.no_sweep:
             line["sweep"] = sweep_table(dev, pk["bf16_sus"])
+        if world == 1 and not args.no_configs:
+            line["configs"] = {c.name: config_measure(c, dev, pk, n, cpu=not args.no_cpu_baseline)
+                               for c, n in ((synth.TINY, 1), (synth.WAN13_480P, 4))}
         if world == 1 and not args.no_cpu_baseline:
             dt, g, thr = oracle_sample(wl, K, args.cpu_seconds)
             val = dt / g * wl.B * wl.H * wl.G * 1e3
@@ -535,9 +712,45 @@ def run_mcs(args, wl, K):
                                     "sample": f"{g} random query groups of one head, reuse-step sparse attention "
                                               f"in float64 numpy ({dt:.1f} s), extrapolated to "
                                               f"{wl.B * wl.H * wl.G} groups"}
+            smp = oracle_anchor_sample(wl, K)
+            ext = oracle_layer_ms(wl, smp)
+            line["cpu_baseline"]["anchor"] = {
+                "value": ext["anchor"], "unit": "ms/layer", "cores": smp["threads"],
+                "sample": f"one head: full grouping ({smp['pddp_s']:.1f} s) + {smp['groups']} sampled groups "
+                          f"(dense rows, LSE, scores, top-K, sparse, residual), float64 numpy, extrapolated to "
+                          f"{wl.B * wl.H} heads x {wl.G} groups"}
+        line["per_config"] = summary(line, wl)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def summary(line, wl):
+    """Compact per-config digest, printed last in the JSON line: ms per stage,
+    the reuse kernel's kept TFLOP/s and roofline fraction, its speedup over the
+    dense kernel, and the oracle's time on the host cores."""
+    out = {}
+    for name, c in (line.get("configs") or {}).items():
+        cb = c.get("cpu_baseline") or {}
+        out[name] = {"stages_ms": {k: _r(v) for k, v in c["stages_ms"].items()}, "sparse_tflops": _r(c["sparse_tflops"]),
+                     "frac": _r(c["frac"], 3), "speedup": _r(c["speedup_vs_dense"], 3),
+                     "cpu_ms": {"anchor": _r(cb.get("anchor_ms")), "reuse": _r(cb.get("reuse_ms"))}}
+    cb = line.get("cpu_baseline") or {}
+    out[wl.name] = {"stages_ms": {k: _r(v) for k, v in line["stages_ms"].items()}, "sparse_tflops": _r(line["tflops"]),
+                    "frac": _r(line["roofline"]["frac"], 3), "speedup": _r(line["speedup_vs_dense"], 3),
+                    "cpu_ms": {"anchor": _r((cb.get("anchor") or {}).get("value")), "reuse": _r(cb.get("value"))}}
+    ao = line.get("anchor_overhead")
+    if ao:
+        out[ao["workload"]] = {rho: {"total_ms": _r(v["total_ms"]), "overhead_pts": _r(v["anchor_overhead_points"], 3),
+                                     "floor_pts": _r(v["floor_points_dense_anchor_ideal_reuse"], 3),
+                                     "reuse_tflops": _r(v["reuse_tflops"]), "frac": _r(v["reuse_frac"], 3),
+                                     "vs_dense": _r(v["vs_all_dense"], 3)}
+                               for rho, v in ao.items() if isinstance(v, dict) and "total_ms" in v}
+    sw = line.get("sweep")
+    if sw:
+        out[sw["workload"]] = {shape: {"frac": t["frac"], "speedup": [_r(x, 3) for x in t["speedup_vs_dense"]]}
+                               for shape, t in sw["by_shape"].items()}
+    return out
 
 
 def main():

@@ -55,7 +55,8 @@ typedef struct CUstream_st *mcs_stream; /* same type as cudaStream_t */
 typedef enum {
   MCS_OK = 0,
   MCS_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad size, K out of [1, N] */
-  MCS_ERR_UNSUPPORTED = 2,    /* d, C or dtype outside the supported set */
+  MCS_ERR_UNSUPPORTED = 2,    /* d, C or dtype outside the supported set, or (mcs_anchor_select_noalloc)
+                                 N too large for one score row in its fixed array */
   MCS_ERR_WORKSPACE = 3,      /* workspace pointer null or smaller than mcs_workspace_size() */
   MCS_ERR_CUDA = 4,           /* a CUDA runtime call or kernel launch failed */
   MCS_ERR_DEVICE_BOUNDS = 5,  /* a kernel met an index outside [0, N) (reported by mcs_check_status) */
@@ -241,6 +242,17 @@ uint64_t mcs_launch_count(void);
  * pointers. */
 mcs_status mcs_selftest_tc_mma(const void *a, const void *b, float *d, int mode, uint32_t mn_lbo, uint32_t mn_sbo,
                                mcs_stream stream);
+
+/* Diagnostic (no counterpart in the method): the failure path of the library's
+ * bounded waits. Every pipeline wait inside the kernels (a stage that a copy or
+ * an MMA should fill) gives up after a wall-time limit, raises the timeout flag,
+ * lets its own copies land, frees its tensor memory and returns, instead of
+ * hanging the GPU. This launches one CTA that holds tensor memory and waits on a
+ * barrier nothing arrives at, with a limit of limit_ns (1 ns .. 10 s), so the
+ * path can be exercised: afterwards mcs_check_status() returns
+ * MCS_ERR_DEVICE_TIMEOUT (once) and the context stays usable. elapsed_ns: device
+ * uint64 receiving the wait's duration in ns, or NULL. */
+mcs_status mcs_selftest_wait_timeout(uint64_t limit_ns, uint64_t *elapsed_ns, mcs_stream stream);
 
 /* Diagnostic (no counterpart in the method): gathers 128 rows of the bf16 matrix
  * src [nrows x 128] (row-major, device) with TMA 4-row gathers into the swizzled

@@ -65,13 +65,18 @@ def principal_direction(xc: np.ndarray, iters: int) -> np.ndarray:
     return v
 
 
-def pddp_groups(x: np.ndarray, n_real: int, C: int, iters: int = 20):
+def pddp_groups(x: np.ndarray, n_real: int, C: int, iters: int = 20, trace: list | None = None):
     """PDDP grouping of one head's queries into G = ceil(N/C) groups of exactly C.
 
     x is [N_pad, d] (rows >= n_real are pads and are ignored). Recursive
     principal-direction split at the rank floor(n/2)*C [grouping].
     Returns (perm [N_pad] int64: token ids group by group, ascending within a
     group; group_of [n_real] int64).
+    trace: if a list is given, one record per split node is appended (a report
+    only; it changes nothing): g0 (first group id of the node), n (groups),
+    left (sorted member ids sent left) and gap (the key gap at the rank split,
+    key[n_left*C] - key[n_left*C - 1] among the sorted keys, divided by the
+    standard deviation of the node's real keys; inf when the split is at a pad).
     """
     N_pad = x.shape[0]
     assert N_pad % C == 0 and N_pad - n_real < C and n_real > 0
@@ -90,6 +95,12 @@ def pddp_groups(x: np.ndarray, n_real: int, C: int, iters: int = 20):
         n_left = n // 2
         left = np.sort(members[order[: n_left * C]])
         right = np.sort(members[order[n_left * C:]])
+        if trace is not None:
+            ks = key[order]
+            sd = float(np.std(proj[members < n_real]))
+            gap = float(ks[n_left * C] - ks[n_left * C - 1])
+            trace.append(dict(g0=len(groups), n=n, left=left,
+                              gap=gap / sd if np.isfinite(gap) and sd > 0 else math.inf))
         split(left, n_left)
         split(right, n - n_left)
 

@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "mcs.h"
+#include "api_internal.h"
 #include "attn_tc.h"
 #include "common.cuh"
 #include "kernels.h"
@@ -170,6 +171,76 @@ mcs_status sparse_impl(const Dims& dm, int epi, const void* q, const void* k, co
 }  // namespace
 
 namespace mcs {
+mcs_status anchor_select_rows(const mcs_desc* desc, const void* q, const void* k, const int32_t* perm,
+                              const float* lse, int K, int32_t* idx, float* mass, float* scores, size_t score_bytes,
+                              cudaStream_t s) {
+  Dims dm;
+  mcs_status st = check_desc(desc, &dm);
+  if (st != MCS_OK) return st;
+  if (K < 1 || K > dm.N) return MCS_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(perm) || !aligned16(idx) || !aligned16(lse))
+    return MCS_ERR_INVALID_ARG;
+  if (!aligned16_or_null(mass) || !aligned16(scores)) return MCS_ERR_INVALID_ARG;
+  // score rows per launch: what fits, at most kSelectRows (the launch grids stay small)
+  const long long rows = std::min<long long>(kSelectRows, static_cast<long long>(score_bytes / (size_t(dm.N) * 4)));
+  if (rows < 1) return MCS_ERR_UNSUPPORTED;
+  uint32_t* status = nullptr;
+  if ((st = device_state(&status, nullptr)) != MCS_OK) return st;
+  const long long total = static_cast<long long>(dm.BH) * dm.G;
+  for (long long r0 = 0; r0 < total; r0 += rows) {
+    const int nrows = static_cast<int>(std::min<long long>(rows, total - r0));
+    cudaError_t e;
+    if (dm.bf16) {
+      TcColsumParams p{};
+      p.q = static_cast<const __nv_bfloat16*>(q);
+      p.k = static_cast<const __nv_bfloat16*>(k);
+      p.perm = perm;
+      p.lse = lse;
+      p.scores = scores;
+      p.BH = dm.BH;
+      p.N = dm.N;
+      p.N_pad = dm.N_pad;
+      p.C = dm.C;
+      p.G = dm.G;
+      p.row0 = static_cast<int>(r0);
+      p.scale_log2 = dm.scale * kLog2e;
+      p.status = status;
+      e = tc_colsum(dm.d, dm.C, p, nrows, s);
+    } else {
+      SimtColsumParams p{};
+      p.q = static_cast<const float*>(q);
+      p.k = static_cast<const float*>(k);
+      p.perm = perm;
+      p.lse = lse;
+      p.scores = scores;
+      p.N = dm.N;
+      p.N_pad = dm.N_pad;
+      p.C = dm.C;
+      p.G = dm.G;
+      p.d = dm.d;
+      p.row0 = static_cast<int>(r0);
+      p.scale = dm.scale;
+      p.status = status;
+      e = simt_colsum(p, nrows, s);
+    }
+    if (e != cudaSuccess) return MCS_ERR_CUDA;
+    TopkParams t{};
+    t.scores = scores;
+    t.perm = perm;
+    t.idx = idx;
+    t.mass = mass;
+    t.N = dm.N;
+    t.N_pad = dm.N_pad;
+    t.C = dm.C;
+    t.G = dm.G;
+    t.K = K;
+    t.row0 = static_cast<int>(r0);
+    t.status = status;
+    if ((e = topk_rows(t, nrows, s)) != cudaSuccess) return MCS_ERR_CUDA;
+  }
+  return MCS_OK;
+}
+
 void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 uint32_t* status_word_for_current_device() {
   uint32_t* st = nullptr;
@@ -241,67 +312,16 @@ mcs_status mcs_anchor_select(const mcs_desc* desc, const void* q, const void* k,
   if ((st = device_state(&status, nullptr)) != MCS_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
+  const size_t lse_bytes = align256(size_t(dm.BH) * dm.N * 4);
   float* ws_lse = reinterpret_cast<float*>(w);
-  float* scores = reinterpret_cast<float*>(w + align256(size_t(dm.BH) * dm.N * 4));
+  float* scores = reinterpret_cast<float*>(w + lse_bytes);
   if (lse == nullptr) {
     // pass 1 computed here: row max / log-sum-exp only (no P V product)
     st = dense_impl(dm, q, k, k, nullptr, ws_lse, status, s);
     if (st != MCS_OK) return st;
     lse = ws_lse;
   }
-  const long long total = static_cast<long long>(dm.BH) * dm.G;
-  for (long long r0 = 0; r0 < total; r0 += kSelectRows) {
-    const int nrows = static_cast<int>(std::min<long long>(kSelectRows, total - r0));
-    cudaError_t e;
-    if (dm.bf16) {
-      mcs::TcColsumParams p{};
-      p.q = static_cast<const __nv_bfloat16*>(q);
-      p.k = static_cast<const __nv_bfloat16*>(k);
-      p.perm = perm;
-      p.lse = lse;
-      p.scores = scores;
-      p.BH = dm.BH;
-      p.N = dm.N;
-      p.N_pad = dm.N_pad;
-      p.C = dm.C;
-      p.G = dm.G;
-      p.row0 = static_cast<int>(r0);
-      p.scale_log2 = dm.scale * mcs::kLog2e;
-      p.status = status;
-      e = mcs::tc_colsum(dm.d, dm.C, p, nrows, s);
-    } else {
-      mcs::SimtColsumParams p{};
-      p.q = static_cast<const float*>(q);
-      p.k = static_cast<const float*>(k);
-      p.perm = perm;
-      p.lse = lse;
-      p.scores = scores;
-      p.N = dm.N;
-      p.N_pad = dm.N_pad;
-      p.C = dm.C;
-      p.G = dm.G;
-      p.d = dm.d;
-      p.row0 = static_cast<int>(r0);
-      p.scale = dm.scale;
-      p.status = status;
-      e = mcs::simt_colsum(p, nrows, s);
-    }
-    if (e != cudaSuccess) return MCS_ERR_CUDA;
-    mcs::TopkParams t{};
-    t.scores = scores;
-    t.perm = perm;
-    t.idx = idx;
-    t.mass = mass;
-    t.N = dm.N;
-    t.N_pad = dm.N_pad;
-    t.C = dm.C;
-    t.G = dm.G;
-    t.K = K;
-    t.row0 = static_cast<int>(r0);
-    t.status = status;
-    if ((e = mcs::topk_rows(t, nrows, s)) != cudaSuccess) return MCS_ERR_CUDA;
-  }
-  return MCS_OK;
+  return mcs::anchor_select_rows(desc, q, k, perm, lse, K, idx, mass, scores, ws_bytes - lse_bytes, s);
 }
 
 mcs_status mcs_sparse_attn_gather(const mcs_desc* desc, const void* q, const void* k, const void* v,
@@ -508,6 +528,16 @@ mcs_status mcs_selftest_tc_mma(const void* a, const void* b, float* d, int mode,
   mcs_status st = device_state(&status, nullptr);
   if (st != MCS_OK) return st;
   return from_cuda(mcs::tc_probe(a, b, d, mode, mn_lbo, mn_sbo, status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mcs_status mcs_selftest_wait_timeout(uint64_t limit_ns, uint64_t* elapsed_ns, mcs_stream stream) {
+  if (limit_ns == 0 || limit_ns > 10ull * 1000 * 1000 * 1000) return MCS_ERR_INVALID_ARG;
+  if (elapsed_ns != nullptr && (reinterpret_cast<uintptr_t>(elapsed_ns) & 7u) != 0) return MCS_ERR_INVALID_ARG;
+  uint32_t* status = nullptr;
+  mcs_status st = device_state(&status, nullptr);
+  if (st != MCS_OK) return st;
+  return from_cuda(mcs::wait_timeout_probe(limit_ns, reinterpret_cast<unsigned long long*>(elapsed_ns), status,
+                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mcs_status mcs_selftest_tma_gather(const void* src, int nrows, const int32_t* rows, void* out, mcs_stream stream) {

@@ -138,6 +138,7 @@ __global__ void __launch_bounds__(128) simt_colsum_kernel(const SimtColsumParams
   }
   for (int i = threadIdx.x; i < p.C; i += blockDim.x) {
     const int t = p.perm[size_t(bh) * p.N_pad + size_t(g) * p.C + i];
+    if ((t < 0 || t >= p.N_pad) && blockIdx.x == 0) raise_status(p.status, kStatusBounds);
     lse[i] = (t >= 0 && t < p.N) ? p.lse[size_t(bh) * p.N + t] : INFINITY;
   }
   __syncthreads();

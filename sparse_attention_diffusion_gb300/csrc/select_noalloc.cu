@@ -15,13 +15,10 @@
 // previous call's contents; every score the top-K reads is written earlier in
 // the same call, so nothing has to be cleared first. Calls whose kernels overlap
 // on the GPU (different streams, or different host threads) race on it.
-#include <cmath>
 #include <mutex>
 
 #include "mcs.h"
-#include "attn_tc.h"
-#include "common.cuh"
-#include "kernels.h"
+#include "api_internal.h"
 
 namespace {
 
@@ -54,76 +51,14 @@ bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr
 extern "C" mcs_status mcs_anchor_select_noalloc(const mcs_desc* desc, const void* q, const void* k,
                                                 const int32_t* perm, const float* lse, int K, int32_t* idx,
                                                 float* mass, mcs_stream stream) {
-  if (desc == nullptr || desc->B < 1 || desc->H < 1 || desc->N < 1) return MCS_ERR_INVALID_ARG;
-  if ((desc->d != 64 && desc->d != 128) || (desc->C != 64 && desc->C != 128)) return MCS_ERR_UNSUPPORTED;
-  if (desc->dtype != MCS_F32 && desc->dtype != MCS_BF16) return MCS_ERR_UNSUPPORTED;
-  if (!std::isfinite(desc->scale)) return MCS_ERR_INVALID_ARG;
-  const long long N = desc->N, C = desc->C, d = desc->d;
-  const long long G = (N + C - 1) / C, BH = static_cast<long long>(desc->B) * desc->H;
-  if (BH > 65535 || BH * G * C >= (1ll << 31)) return MCS_ERR_UNSUPPORTED;
-  // one score row of N fp32 values must fit in the fixed scratch array
-  const long long rows_fit = static_cast<long long>(kScratchBytes) / (N * 4);
-  if (rows_fit < 1) return MCS_ERR_UNSUPPORTED;
-  if (K < 1 || K > N) return MCS_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(perm) || !aligned16(idx) || !aligned16(lse))
-    return MCS_ERR_INVALID_ARG;  // lse (pass 1) is required here: it is not computed into scratch
-  if (mass != nullptr && !aligned16(mass)) return MCS_ERR_INVALID_ARG;
+  // argument checks (lse is required: pass 1 is not computed into the array) and
+  // the launch loop are those of the workspace entry point; score rows per
+  // launch are what fits in the array, at most 4,096
+  if (desc == nullptr || desc->N < 1) return MCS_ERR_INVALID_ARG;
+  if (static_cast<long long>(kScratchBytes) / (static_cast<long long>(desc->N) * 4) < 1) return MCS_ERR_UNSUPPORTED;
+  if (!aligned16(lse)) return MCS_ERR_INVALID_ARG;
   float* scores = scratch_for_current_device();
-  uint32_t* status = mcs::status_word_for_current_device();
-  if (scores == nullptr || status == nullptr) return MCS_ERR_CUDA;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const float scale = desc->scale > 0.f ? desc->scale : 1.0f / sqrtf(static_cast<float>(d));
-  const long long total = BH * G;
-  for (long long r0 = 0; r0 < total; r0 += rows_fit) {
-    const int nrows = static_cast<int>(total - r0 < rows_fit ? total - r0 : rows_fit);
-    cudaError_t e;
-    if (desc->dtype == MCS_BF16) {
-      mcs::TcColsumParams p{};
-      p.q = static_cast<const __nv_bfloat16*>(q);
-      p.k = static_cast<const __nv_bfloat16*>(k);
-      p.perm = perm;
-      p.lse = lse;
-      p.scores = scores;
-      p.BH = static_cast<int>(BH);
-      p.N = static_cast<int>(N);
-      p.N_pad = static_cast<int>(G * C);
-      p.C = static_cast<int>(C);
-      p.G = static_cast<int>(G);
-      p.row0 = static_cast<int>(r0);
-      p.scale_log2 = scale * mcs::kLog2e;
-      p.status = status;
-      e = mcs::tc_colsum(static_cast<int>(d), static_cast<int>(C), p, nrows, s);
-    } else {
-      mcs::SimtColsumParams p{};
-      p.q = static_cast<const float*>(q);
-      p.k = static_cast<const float*>(k);
-      p.perm = perm;
-      p.lse = lse;
-      p.scores = scores;
-      p.N = static_cast<int>(N);
-      p.N_pad = static_cast<int>(G * C);
-      p.C = static_cast<int>(C);
-      p.G = static_cast<int>(G);
-      p.d = static_cast<int>(d);
-      p.row0 = static_cast<int>(r0);
-      p.scale = scale;
-      p.status = status;
-      e = mcs::simt_colsum(p, nrows, s);
-    }
-    if (e != cudaSuccess) return MCS_ERR_CUDA;
-    mcs::TopkParams t{};
-    t.scores = scores;
-    t.perm = perm;
-    t.idx = idx;
-    t.mass = mass;
-    t.N = static_cast<int>(N);
-    t.N_pad = static_cast<int>(G * C);
-    t.C = static_cast<int>(C);
-    t.G = static_cast<int>(G);
-    t.K = K;
-    t.row0 = static_cast<int>(r0);
-    t.status = status;
-    if (mcs::topk_rows(t, nrows, s) != cudaSuccess) return MCS_ERR_CUDA;
-  }
-  return MCS_OK;
+  if (scores == nullptr) return MCS_ERR_CUDA;
+  return mcs::anchor_select_rows(desc, q, k, perm, lse, K, idx, mass, scores, kScratchBytes,
+                                 reinterpret_cast<cudaStream_t>(stream));
 }

@@ -136,7 +136,48 @@ __global__ void __launch_bounds__(128, 1) tma_gather_probe_kernel(const __grid_c
     *reinterpret_cast<uint4*>(out + tid * 128 + ch * 8) = *reinterpret_cast<const uint4*>(tile + sw128_off(tid, ch));
 }
 
+// Waits on an mbarrier that nothing ever arrives at, with a wait limit of
+// limit_ns, the way every pipeline wait in the library is bounded: the wait
+// gives up, the kernel raises the timeout flag, releases the tensor memory it
+// holds and returns, so the context stays usable. elapsed (nullable) receives
+// the nanoseconds thread 0 spent waiting.
+__global__ void __launch_bounds__(128, 1) wait_timeout_probe_kernel(uint64_t limit_ns, unsigned long long* elapsed,
+                                                                    uint32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t slot;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) {
+    mbar_init(&bar, 1);  // one arrival expected, none ever made
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&slot, 32);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = slot;
+  const uint64_t t0 = globaltimer_ns();
+  const bool ok = mbar_wait(&bar, 0, status, limit_ns);
+  const uint64_t t1 = globaltimer_ns();
+  if (!ok && tid == 0) raise_status(status, kStatusTimeout);
+  if (tid == 0 && elapsed != nullptr) *elapsed = static_cast<unsigned long long>(t1 - t0);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 32);
+  }
+}
+
 }  // namespace
+
+cudaError_t wait_timeout_probe(uint64_t limit_ns, unsigned long long* elapsed, uint32_t* status, cudaStream_t stream) {
+  wait_timeout_probe_kernel<<<1, 128, 0, stream>>>(limit_ns, elapsed, status);
+  note_launches(1);
+  return cudaGetLastError();
+}
 
 cudaError_t tma_gather_probe(const void* src, int nrows, const int* rows, void* out, uint32_t* status,
                              cudaStream_t stream) {

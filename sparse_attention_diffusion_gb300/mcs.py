@@ -25,7 +25,8 @@ EXPORTS = ("mcs_workspace_size", "mcs_group_pddp", "mcs_dense_attn", "mcs_anchor
            "mcs_check_status", "mcs_status_string", "mcs_launch_count", "mcs_selftest_tc_mma",
            "mcs_selftest_tma_gather", "mcs_anchor_select_noalloc", "mcs_sparse_attn_gather_host",
            "mcs_sparse_attn_gather_host_workspace_size", "mcs_cache_entry_bytes", "mcs_cache_ring_create",
-           "mcs_cache_ring_acquire", "mcs_cache_ring_release", "mcs_cache_ring_destroy")
+           "mcs_cache_ring_acquire", "mcs_cache_ring_release", "mcs_cache_ring_destroy",
+           "mcs_selftest_wait_timeout")
 
 
 class McsError(RuntimeError):
@@ -73,6 +74,7 @@ def load(build_if_missing: bool = False):
         "mcs_launch_count": (ctypes.c_uint64, []),
         "mcs_selftest_tc_mma": (I, [P, P, P, I, ctypes.c_uint32, ctypes.c_uint32, S]),
         "mcs_selftest_tma_gather": (I, [P, I, P, P, S]),
+        "mcs_selftest_wait_timeout": (I, [ctypes.c_uint64, P, S]),
         "mcs_anchor_select_noalloc": (I, [D, P, P, P, P, I, P, P, S]),
         "mcs_sparse_attn_gather_host": (I, [D, P, P, P, P, P, I, P, P, P, Z, I, S]),
         "mcs_sparse_attn_gather_host_workspace_size": (Z, [D, I]),
@@ -312,6 +314,13 @@ def mcs_launch_count() -> int:
 def mcs_selftest_tc_mma(a, b, d, mode, mn_lbo=16384, mn_sbo=1024, stream=None):
     _check("mcs_selftest_tc_mma", load().mcs_selftest_tc_mma(_ptr(a), _ptr(b), _ptr(d), int(mode), int(mn_lbo),
                                                              int(mn_sbo), _stream(stream)))
+
+
+def mcs_selftest_wait_timeout(limit_ns, elapsed=None, stream=None):
+    """Launch the bounded-wait diagnostic (a wait that must time out after limit_ns).
+    elapsed: optional int64 device tensor of one element receiving the wait in ns."""
+    _check("mcs_selftest_wait_timeout", load().mcs_selftest_wait_timeout(int(limit_ns), _ptr(elapsed),
+                                                                         _stream(stream)))
 
 
 def mcs_selftest_tma_gather(src, rows, out, stream=None):

@@ -1,11 +1,14 @@
 """The meta-cache ring: anchor entries written into a device slot and copied out
 to host memory, then brought back (with the next layer prefetched) for reuse
 steps, give bit for bit the reuse outputs of caches that never left the
-device; acquire/release out of order is refused."""
+device, and those outputs match the float64 oracle's reuse step run on the
+entry the ring brought back; acquire/release out of order is refused."""
 import pytest
 import torch
 
+from oracle import mcs_oracle as orc
 from sparse_attention_diffusion_gb300 import mcs, synth
+from tests import parity
 
 pytestmark = pytest.mark.gpu
 
@@ -56,17 +59,27 @@ def test_ring_round_trip_matches_resident_caches(layers):
             _anchor(desc, K, *L["qkv"], c["perm"], c["idx"], c["residual"])
             ring.release(l, store=True)
         for rnd in range(2):                          # reuse steps: entries from host, next layer prefetched
-            outs = []
+            outs, entries = [], []
             for l, L in enumerate(layers):
                 c = ring.acquire(l, fill=True, prefetch_next=True)
                 o = torch.empty_like(L["want"])
                 mcs.mcs_sparse_attn_gather(desc, *L["qkv2"], c["perm"], c["idx"], K, c["residual"], o)
+                if rnd == 0:   # the entry as the kernel read it (copied before the slot is released)
+                    entries.append({n: c[n].cpu() for n in ("perm", "idx", "residual")})
                 ring.release(l)
                 outs.append(o)
             torch.cuda.synchronize()
             mcs.mcs_check_status()
             for l, (o, L) in enumerate(zip(outs, layers)):
                 assert torch.equal(o, L["want"]), f"pass {rnd} layer {l}: ring cache differs from resident cache"
+            # the reuse step against the float64 oracle, fed the entry the ring brought back
+            for l, (o, L, e) in enumerate(zip(outs, layers, entries)):
+                for h in range(desc.H):
+                    q2, k2, v2 = (parity.f64(t[0, h]) for t in L["qkv2"])
+                    want = orc.reuse_head(q2, k2, v2, e["perm"][0, h].numpy(), e["idx"][0, h].numpy(),
+                                          parity.f64(e["residual"][0, h]), desc.C)
+                    parity.assert_close(parity.f64(o[0, h]), want, "bf16" if L["dtype"] == torch.bfloat16 else "f32",
+                                        f"layer {l} head {h}: ring reuse output vs oracle")
     finally:
         ring.close()
 

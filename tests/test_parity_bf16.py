@@ -77,16 +77,18 @@ def test_groups(run):
     for b, h in _heads(run):
         x = np.zeros((wl.N_pad, wl.d))
         x[:wl.N] = parity.f64(run["q"][b, h])
-        perm_ref, _ = orc.pddp_groups(x, wl.N, wl.C, 20)
         perm = run["cache"]["perm"][b, h].cpu().numpy()
         parity.assert_valid_partition(perm, wl.N, wl.C)
         group_of = run["cache"]["group_of"][b, h].cpu().numpy()
         for g in range(wl.G):
             mem = parity.group_members(perm, g, wl.C, wl.N)
             assert np.all(group_of[mem] == g)
-        agree = parity.pddp_agreement(perm, perm_ref, wl.C)
-        print(f"PDDP group agreement head {b},{h}: {agree:.3f}")
-        assert agree >= 0.5
+        agree, _, bad = parity.pddp_split_report(perm, x, wl.N, wl.C)
+        gaps = ", ".join(f"g0={s['g0']} n={s['n']} gap {s['gap']:.2e} sd moved {s['moved']}" for s in bad)
+        print(f"PDDP group agreement head {b},{h}: {agree:.3f} [{gaps}]")
+        assert agree >= parity.PDDP_AGREE_FLOOR_SMALL, f"head {b},{h}: agreement {agree:.3f}"
+        for s in bad:
+            assert s["gap"] <= parity.PDDP_GAP_MAX, f"head {b},{h}: disagreeing split with oracle gap {s['gap']:.3g} sd"
 
 
 def test_selection(run):
