@@ -342,11 +342,16 @@ def matched_density(desc, K, q, k, v, o_dense, cache, ws):
     return out
 
 
-def schedule_overhead(dev, peak_tflops):
+def schedule_overhead(dev, peak_tflops, warm_iters=4):
     """The full meta-cache schedule on the 118,800-token layer (24 heads, 50 steps:
     5 dense warm-up steps, an anchor every 10 steps, reuse steps otherwise, drift
     0.05) at densities 0.15 and 0.25: total time including anchors and the anchor
-    cost as equivalent extra density (post-warm-up time over 45 dense steps)."""
+    cost as equivalent extra density (post-warm-up time over 45 dense steps).
+    Each density runs twice: grouping every anchor from the fixed start, and the
+    amortised ("fast PDDP") grouping that starts each node from the previous
+    anchor's direction with `warm_iters` iterations (`fast_pddp`: its grouping
+    time, overhead, and the anchors' mean captured attention mass beside the
+    cold run's)."""
     import torch
 
     from sparse_attention_diffusion_gb300 import mcs, schedule, synth
@@ -354,14 +359,20 @@ def schedule_overhead(dev, peak_tflops):
     out = {"workload": synth.SCHEDULE_HY.name, "steps": 50, "warmup": 5, "period": 10}
     for rho in ("0.15", "0.25"):
         wl = synth.SCHEDULE_HY.with_(density=rho)
-        layer = synth.make_layer(wl, device=dev)
-        q0, _, _ = layer.cast()
-        desc = mcs.desc_for(q0, wl.C)
-        ml = schedule.MetaCacheLayer(desc, wl.K, q0.dtype, dev)
-        del q0
-        recs = schedule.run(ml, schedule.Schedule(steps=50, warmup=5, period=10), layer.cast,
-                            lambda: layer.drift_step())
-        mcs.mcs_check_status()
+        res = {}
+        for mode in ("cold", "warm"):
+            layer = synth.make_layer(wl, device=dev)
+            q0, _, _ = layer.cast()
+            desc = mcs.desc_for(q0, wl.C)
+            ml = schedule.MetaCacheLayer(desc, wl.K, q0.dtype, dev, warm_iters=warm_iters if mode == "warm" else None)
+            del q0
+            recs = schedule.run(ml, schedule.Schedule(steps=50, warmup=5, period=10), layer.cast,
+                                lambda: layer.drift_step())
+            mcs.mcs_check_status()
+            res[mode] = (recs, ml.masses)
+            del ml, layer
+            torch.cuda.empty_cache()
+        recs = res["cold"][0]
         t_dense = statistics.median(r.ms for r in recs[1:5])  # the first dense step pays one-off costs
         rho_eq, extra = schedule.anchor_overhead(recs, t_dense, float(wl.density), 5)
         kinds = {k: [r.ms for r in recs if r.kind == k] for k in ("dense", "anchor", "reuse")}
@@ -369,6 +380,9 @@ def schedule_overhead(dev, peak_tflops):
         n_anchor, n_reuse = len(kinds["anchor"]), len(kinds["reuse"])
         t_reuse = statistics.mean(kinds["reuse"])
         reuse_tf = flops_sparse(wl, wl.K) / (t_reuse * 1e-3) / 1e12
+        wrecs, wmass = res["warm"]
+        w_rho_eq, w_extra = schedule.anchor_overhead(wrecs, t_dense, float(wl.density), 5)
+        w_anchor = [r for r in wrecs if r.kind == "anchor"]
         out[rho] = {"K": wl.K, "total_ms": sum(r.ms for r in recs), "post_warmup_ms": sum(r.ms for r in recs[5:]),
                     "dense_step_ms": t_dense, "anchor_step_ms": statistics.mean(kinds["anchor"]),
                     "anchor_stages_ms": {n: statistics.mean(r.stages[n] for r in recs if r.kind == "anchor")
@@ -380,9 +394,13 @@ def schedule_overhead(dev, peak_tflops):
                     # the same with the measured reuse steps
                     "floor_points_dense_anchor_measured_reuse":
                         100.0 * ((n_anchor * t_dense + n_reuse * t_reuse) / (n_post * t_dense) - float(rho)),
-                    "vs_all_dense": 50 * t_dense / sum(r.ms for r in recs)}
-        del ml, layer, recs
-        torch.cuda.empty_cache()
+                    "vs_all_dense": 50 * t_dense / sum(r.ms for r in recs),
+                    "anchor_mass_mean": statistics.mean(res["cold"][1]),
+                    "fast_pddp": {"warm_iters": warm_iters, "total_ms": sum(r.ms for r in wrecs),
+                                  "anchor_overhead_points": 100.0 * w_extra,
+                                  "pddp_ms_first_anchor": w_anchor[0].stages["pddp"],
+                                  "pddp_ms_warm_anchors": statistics.mean(r.stages["pddp"] for r in w_anchor[1:]),
+                                  "anchor_mass_mean": statistics.mean(wmass)}}
     return out
 
 
@@ -744,7 +762,12 @@ def summary(line, wl):
         out[ao["workload"]] = {rho: {"total_ms": _r(v["total_ms"]), "overhead_pts": _r(v["anchor_overhead_points"], 3),
                                      "floor_pts": _r(v["floor_points_dense_anchor_ideal_reuse"], 3),
                                      "reuse_tflops": _r(v["reuse_tflops"]), "frac": _r(v["reuse_frac"], 3),
-                                     "vs_dense": _r(v["vs_all_dense"], 3)}
+                                     "vs_dense": _r(v["vs_all_dense"], 3),
+                                     "pddp_ms": _r(v["anchor_stages_ms"]["pddp"], 3),
+                                     "mass": _r(v["anchor_mass_mean"], 4),
+                                     "fast_pddp": {"overhead_pts": _r(v["fast_pddp"]["anchor_overhead_points"], 3),
+                                                   "pddp_ms": _r(v["fast_pddp"]["pddp_ms_warm_anchors"], 3),
+                                                   "mass": _r(v["fast_pddp"]["anchor_mass_mean"], 4)}}
                                for rho, v in ao.items() if isinstance(v, dict) and "total_ms" in v}
     sw = line.get("sweep")
     if sw:

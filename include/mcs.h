@@ -93,6 +93,26 @@ size_t mcs_workspace_size(const mcs_desc *desc, int K);
 mcs_status mcs_group_pddp(const mcs_desc *desc, const void *q, int32_t *perm, int32_t *group_of,
                           void *ws, size_t ws_bytes, mcs_stream stream);
 
+/* [grouping] "Fast PDDP": the same grouping with the power iteration of every
+ * tree node started from a stored direction instead of 1/sqrt(d)*ones. The
+ * pages report the grouping's cost amortised over the denoising steps without
+ * describing how; this is the plainest reading: an anchor starts each node from
+ * the direction the previous anchor found for it (the queries drift little
+ * between anchors), so a few iterations (desc->pddp_iters, e.g. 4) do the work
+ * of 20 from the fixed start.
+ * Direction tables are fp32 [B, H, S, d] with S = 2^ceil(log2 G) - 1 rows per
+ * head: tree node k of level l (root: level 0; the children of node k are
+ * nodes 2k and 2k+1 of the next level) is row 2^l - 1 + k; rows of nodes that
+ * do not split are unused. mcs_pddp_dirs_size() gives the bytes of one table
+ * (0 for an invalid description). dirs_in: start directions or NULL (then
+ * 1/sqrt(d)*ones, i.e. mcs_group_pddp); dirs_out: receives every split node's
+ * final direction, or NULL; the two may be the same buffer. Iterations:
+ * desc->pddp_iters when > 0; 0 with dirs_in given uses the stored directions
+ * as they are; otherwise 20. Other arguments and results as mcs_group_pddp. */
+size_t mcs_pddp_dirs_size(const mcs_desc *desc);
+mcs_status mcs_group_pddp_warm(const mcs_desc *desc, const void *q, const float *dirs_in, float *dirs_out,
+                               int32_t *perm, int32_t *group_of, void *ws, size_t ws_bytes, mcs_stream stream);
+
 /* [dense] + [selection] pass 1: full softmax attention of every query over every
  * key, o_i = sum_j softmax_j(scale q_i.k_j) v_j, and the row log-sum-exp.
  * q, k, v: [B,H,N,d] inputs; o: [B,H,N,d] output (may be NULL to compute only

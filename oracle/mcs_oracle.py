@@ -39,7 +39,7 @@ import math
 import numpy as np
 
 __all__ = [
-    "principal_direction", "pddp_groups", "dense_attention", "group_scores",
+    "principal_direction", "pddp_node_slot", "pddp_groups", "dense_attention", "group_scores",
     "topk_ascending", "sparse_attention", "captured_mass", "anchor_head",
     "reuse_head", "default_scale",
 ]
@@ -50,13 +50,14 @@ def default_scale(d: int) -> float:
 
 
 # ---------------------------------------------------------------- [grouping]
-def principal_direction(xc: np.ndarray, iters: int) -> np.ndarray:
+def principal_direction(xc: np.ndarray, iters: int, v0: np.ndarray | None = None) -> np.ndarray:
     """Power iteration on the centred rows xc [n, d]: w = xc^T (xc v), v <- w/|w|.
 
-    Exactly `iters` steps from v = 1/sqrt(d) * ones; a zero w leaves v unchanged.
+    Exactly `iters` steps from v0 (default 1/sqrt(d) * ones); a zero w leaves v
+    unchanged.
     """
     d = xc.shape[1]
-    v = np.full(d, 1.0 / math.sqrt(d))
+    v = np.full(d, 1.0 / math.sqrt(d)) if v0 is None else np.asarray(v0, dtype=np.float64).copy()
     for _ in range(iters):
         w = xc.T @ (xc @ v)
         nrm = math.sqrt(float(w @ w))
@@ -65,7 +66,15 @@ def principal_direction(xc: np.ndarray, iters: int) -> np.ndarray:
     return v
 
 
-def pddp_groups(x: np.ndarray, n_real: int, C: int, iters: int = 20, trace: list | None = None):
+def pddp_node_slot(level: int, k: int) -> int:
+    """Slot of tree node k of `level` in a per-head direction table: nodes are
+    numbered level by level (root 0; the children of node k are 2k and 2k+1 of
+    the next level), so node (level, k) sits at 2^level - 1 + k."""
+    return (1 << level) - 1 + k
+
+
+def pddp_groups(x: np.ndarray, n_real: int, C: int, iters: int = 20, trace: list | None = None,
+                v_init: np.ndarray | None = None, v_out: np.ndarray | None = None):
     """PDDP grouping of one head's queries into G = ceil(N/C) groups of exactly C.
 
     x is [N_pad, d] (rows >= n_real are pads and are ignored). Recursive
@@ -77,18 +86,26 @@ def pddp_groups(x: np.ndarray, n_real: int, C: int, iters: int = 20, trace: list
     left (sorted member ids sent left) and gap (the key gap at the rank split,
     key[n_left*C] - key[n_left*C - 1] among the sorted keys, divided by the
     standard deviation of the node's real keys; inf when the split is at a pad).
+    v_init / v_out: optional direction tables [2^L - 1, d] (L = ceil(log2 G))
+    indexed by pddp_node_slot. With v_init the power iteration of each split
+    node starts from its row instead of 1/sqrt(d)*ones (the warm start of an
+    amortised grouping: the previous anchor's directions, so that fewer
+    iterations are needed); v_out receives every split node's final direction.
     """
     N_pad = x.shape[0]
     assert N_pad % C == 0 and N_pad - n_real < C and n_real > 0
     groups = []
 
-    def split(members: np.ndarray, n: int):
+    def split(members: np.ndarray, n: int, level: int, k: int):
         if n == 1:
             groups.append(np.sort(members))
             return
         real = members[members < n_real]
         mu = x[real].mean(axis=0)
-        v = principal_direction(x[real] - mu, iters)
+        slot = pddp_node_slot(level, k)
+        v = principal_direction(x[real] - mu, iters, None if v_init is None else v_init[slot])
+        if v_out is not None:
+            v_out[slot] = v
         proj = (x[members] - mu) @ v
         key = np.where(members < n_real, proj, np.inf)
         order = np.lexsort((members, key))          # by key, then token index
@@ -101,10 +118,10 @@ def pddp_groups(x: np.ndarray, n_real: int, C: int, iters: int = 20, trace: list
             gap = float(ks[n_left * C] - ks[n_left * C - 1])
             trace.append(dict(g0=len(groups), n=n, left=left,
                               gap=gap / sd if np.isfinite(gap) and sd > 0 else math.inf))
-        split(left, n_left)
-        split(right, n - n_left)
+        split(left, n_left, level + 1, 2 * k)
+        split(right, n - n_left, level + 1, 2 * k + 1)
 
-    split(np.arange(N_pad), N_pad // C)
+    split(np.arange(N_pad), N_pad // C, 0, 0)
     perm = np.concatenate(groups)
     group_of = np.empty(n_real, dtype=np.int64)
     for g, mem in enumerate(groups):

@@ -259,12 +259,19 @@ size_t mcs_workspace_size(const mcs_desc* desc, int K) {
   return a > b ? a : b;
 }
 
-mcs_status mcs_group_pddp(const mcs_desc* desc, const void* q, int32_t* perm, int32_t* group_of, void* ws,
-                          size_t ws_bytes, mcs_stream stream) {
+size_t mcs_pddp_dirs_size(const mcs_desc* desc) {
+  Dims dm;
+  if (check_desc(desc, &dm) != MCS_OK) return 0;
+  return size_t(dm.BH) * mcs::pddp_dir_slots(dm.G) * dm.d * sizeof(float);
+}
+
+mcs_status mcs_group_pddp_warm(const mcs_desc* desc, const void* q, const float* dirs_in, float* dirs_out,
+                               int32_t* perm, int32_t* group_of, void* ws, size_t ws_bytes, mcs_stream stream) {
   Dims dm;
   mcs_status st = check_desc(desc, &dm);
   if (st != MCS_OK) return st;
   if (!aligned16(q) || !aligned16(perm) || !aligned16(group_of)) return MCS_ERR_INVALID_ARG;
+  if (!aligned16_or_null(dirs_in) || !aligned16_or_null(dirs_out)) return MCS_ERR_INVALID_ARG;
   if (ws == nullptr || !aligned16(ws) || ws_bytes < mcs_workspace_size(desc, 1)) return MCS_ERR_WORKSPACE;
   uint32_t* status = nullptr;
   int sms = 0;
@@ -280,10 +287,17 @@ mcs_status mcs_group_pddp(const mcs_desc* desc, const void* q, int32_t* perm, in
   p.C = dm.C;
   p.G = dm.G;
   p.d = dm.d;
-  p.iters = dm.iters;
+  p.iters = desc->pddp_iters > 0 ? desc->pddp_iters : (desc->pddp_iters == 0 && dirs_in != nullptr ? 0 : 20);
   p.bf16 = dm.bf16;
   p.status = status;
+  p.dirs_in = dirs_in;
+  p.dirs_out = dirs_out;
   return from_cuda(mcs::pddp_run(p, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mcs_status mcs_group_pddp(const mcs_desc* desc, const void* q, int32_t* perm, int32_t* group_of, void* ws,
+                          size_t ws_bytes, mcs_stream stream) {
+  return mcs_group_pddp_warm(desc, q, nullptr, nullptr, perm, group_of, ws, ws_bytes, stream);
 }
 
 mcs_status mcs_dense_attn(const mcs_desc* desc, const void* q, const void* k, const void* v, void* o, float* lse,

@@ -33,7 +33,14 @@ struct PddpProblem {
   bool bf16;
   int num_sms;
   uint32_t* status;
+  // optional direction tables [BH][2^L - 1][d] fp32 (L = ceil(log2 G)), node
+  // (level, k) at row 2^level - 1 + k: start vectors (warm start) / final
+  // directions; may alias (each row is read before it is written)
+  const float* dirs_in;
+  float* dirs_out;
 };
+// Rows of a PDDP direction table per head: 2^ceil(log2 G) - 1.
+int pddp_dir_slots(int G);
 // Workspace bytes for pddp_run (0 if unsupported).
 size_t pddp_workspace_bytes(int BH, int N_pad, int C, int G, int d, bool bf16);
 cudaError_t pddp_run(const PddpProblem& p, void* ws, size_t ws_bytes, cudaStream_t stream);

@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(256) sum_kernel(const T* __restrict__ x, const
 // 2. node mean, start vector
 template <typename A, int D>
 __global__ void mean_kernel(Tables t, int level, int G, const A* psum, const int* pcnt, A* node_mu, A* node_v,
-                            int max_chunks) {
+                            int max_chunks, const float* dirs_in, int slots) {
   const int k = blockIdx.x, bh = blockIdx.y;
   const size_t to = size_t(level) * G + k;
   if (t.node_n[to] < 2) return;
@@ -225,7 +225,11 @@ __global__ void mean_kernel(Tables t, int level, int G, const A* psum, const int
     cnt += pcnt[size_t(bh) * max_chunks + c0 + c];
   }
   node_mu[(size_t(bh) * G + k) * D + threadIdx.x] = cnt > 0 ? s / A(cnt) : A(0);
-  node_v[(size_t(bh) * G + k) * D + threadIdx.x] = A(1) / sqrt(A(D));
+  // start vector: the stored direction of this node (warm start; level-by-level
+  // slot 2^level - 1 + k) or 1/sqrt(D) * ones
+  node_v[(size_t(bh) * G + k) * D + threadIdx.x] =
+      dirs_in != nullptr ? A(dirs_in[(size_t(bh) * slots + (size_t(1) << level) - 1 + k) * D + threadIdx.x])
+                         : A(1) / sqrt(A(D));
 }
 
 // 3a. per-chunk centred covariance; thread (bi, bj) owns a TB x TB block.
@@ -299,7 +303,8 @@ __global__ void __launch_bounds__(256) cov_kernel(const T* __restrict__ x, const
 // n mu mu^T is subtracted once here.
 template <typename A, int D, bool kRaw>
 __global__ void __launch_bounds__(256) power_kernel(Tables t, int level, int G, const A* pcov, A* node_v, int iters,
-                                                    int max_chunks, const A* node_mu, const int* pcnt) {
+                                                    int max_chunks, const A* node_mu, const int* pcnt, float* dirs_out,
+                                                    int slots) {
   extern __shared__ uint8_t dyn[];
   A* cov = reinterpret_cast<A*>(dyn);  // [D][D]
   A* v = cov + D * D;                  // [D]
@@ -340,7 +345,11 @@ __global__ void __launch_bounds__(256) power_kernel(Tables t, int level, int G, 
     if (threadIdx.x < D && nrm2 > A(0)) v[threadIdx.x] = w[threadIdx.x] / sqrt(nrm2);
     __syncthreads();
   }
-  if (threadIdx.x < D) node_v[(size_t(bh) * G + k) * D + threadIdx.x] = v[threadIdx.x];
+  if (threadIdx.x < D) {
+    node_v[(size_t(bh) * G + k) * D + threadIdx.x] = v[threadIdx.x];
+    if (dirs_out != nullptr)
+      dirs_out[(size_t(bh) * slots + (size_t(1) << level) - 1 + k) * D + threadIdx.x] = float(v[threadIdx.x]);
+  }
 }
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -509,6 +518,7 @@ cudaError_t run_typed(const PddpProblem& p, uint8_t* ws, cudaStream_t s) {
   bufs[w.L & 1] = p.perm;
   bufs[(w.L & 1) ^ 1] = reinterpret_cast<int32_t*>(ws + w.perm_tmp);
   const size_t total = size_t(p.BH) * p.N_pad;
+  const int slots = (1 << w.L) - 1;  // direction-table rows per head
   int nlaunch = 0;
   init_perm_kernel<<<1024, 256, 0, s>>>(bufs[0], p.N_pad, total);
   ++nlaunch;
@@ -548,15 +558,16 @@ cudaError_t run_typed(const PddpProblem& p, uint8_t* ws, cudaStream_t s) {
       e = pddp_moments_tc(x, cur, t.chunk_g0 + size_t(l) * G, t.chunk_ng + size_t(l) * G, nch, p.BH, p.N, p.N_pad,
                           p.C, psum, pcnt, pcov, w.max_chunks, p.status, p.num_sms, s);
       if (e != cudaSuccess) return e;
-      mean_kernel<A, D><<<gn, D, 0, s>>>(t, l, G, psum, pcnt, node_mu, node_v, w.max_chunks);
+      mean_kernel<A, D><<<gn, D, 0, s>>>(t, l, G, psum, pcnt, node_mu, node_v, w.max_chunks, p.dirs_in, slots);
       nlaunch += 1;
     } else {
       sum_kernel<T, A, D><<<gc, 256, 0, s>>>(x, cur, t, l, p.N, p.N_pad, p.C, G, psum, pcnt, w.max_chunks);
-      mean_kernel<A, D><<<gn, D, 0, s>>>(t, l, G, psum, pcnt, node_mu, node_v, w.max_chunks);
+      mean_kernel<A, D><<<gn, D, 0, s>>>(t, l, G, psum, pcnt, node_mu, node_v, w.max_chunks, p.dirs_in, slots);
       cov_kernel<T, A, D><<<gc, 256, 0, s>>>(x, cur, t, l, p.N, p.N_pad, p.C, G, node_mu, pcov, w.max_chunks);
       nlaunch += 3;
     }
-    power_kernel<A, D, kTc><<<gn, 256, power_smem, s>>>(t, l, G, pcov, node_v, p.iters, w.max_chunks, node_mu, pcnt);
+    power_kernel<A, D, kTc><<<gn, 256, power_smem, s>>>(t, l, G, pcov, node_v, p.iters, w.max_chunks, node_mu, pcnt,
+                                                        p.dirs_out, slots);
     keys_kernel<T, A, D, KeyT><<<gc, 256, 0, s>>>(x, cur, t, l, p.N, p.N_pad, p.C, G, node_mu, node_v, keys);
     e = cudaMemcpyAsync(nxt, cur, total * sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
     if (e != cudaSuccess) return e;
@@ -570,6 +581,8 @@ cudaError_t run_typed(const PddpProblem& p, uint8_t* ws, cudaStream_t s) {
 }
 
 }  // namespace
+
+int pddp_dir_slots(int G) { return (1 << num_levels(G)) - 1; }
 
 size_t pddp_workspace_bytes(int BH, int N_pad, int C, int G, int d, bool bf16) {
   return layout(BH, N_pad, C, G, d, bf16).total;

@@ -26,7 +26,7 @@ EXPORTS = ("mcs_workspace_size", "mcs_group_pddp", "mcs_dense_attn", "mcs_anchor
            "mcs_selftest_tma_gather", "mcs_anchor_select_noalloc", "mcs_sparse_attn_gather_host",
            "mcs_sparse_attn_gather_host_workspace_size", "mcs_cache_entry_bytes", "mcs_cache_ring_create",
            "mcs_cache_ring_acquire", "mcs_cache_ring_release", "mcs_cache_ring_destroy",
-           "mcs_selftest_wait_timeout")
+           "mcs_selftest_wait_timeout", "mcs_pddp_dirs_size", "mcs_group_pddp_warm")
 
 
 class McsError(RuntimeError):
@@ -63,6 +63,8 @@ def load(build_if_missing: bool = False):
     sig = {
         "mcs_workspace_size": (Z, [D, I]),
         "mcs_group_pddp": (I, [D, P, P, P, P, Z, S]),
+        "mcs_pddp_dirs_size": (Z, [D]),
+        "mcs_group_pddp_warm": (I, [D, P, P, P, P, P, P, Z, S]),
         "mcs_dense_attn": (I, [D, P, P, P, P, P, S]),
         "mcs_anchor_select": (I, [D, P, P, P, P, I, P, P, P, Z, S]),
         "mcs_sparse_attn_gather": (I, [D, P, P, P, P, P, I, P, P, S]),
@@ -172,6 +174,26 @@ def mcs_group_pddp(desc, q, perm, group_of, ws, stream=None):
     _expect(desc, q=q, perm=perm, group_of=group_of)
     _check("mcs_group_pddp", load().mcs_group_pddp(ctypes.byref(desc), _ptr(q), _ptr(perm), _ptr(group_of), _ptr(ws),
                                                    ws.numel(), _stream(stream)))
+
+
+def pddp_dirs(desc, device="cuda") -> torch.Tensor:
+    """A zeroed PDDP direction table [B, H, S, d] fp32 (S = 2^ceil(log2 G) - 1)."""
+    n = int(load().mcs_pddp_dirs_size(ctypes.byref(desc)))
+    S = n // (4 * desc.B * desc.H * desc.d)
+    return torch.zeros((desc.B, desc.H, S, desc.d), dtype=torch.float32, device=device)
+
+
+def mcs_group_pddp_warm(desc, q, dirs_in, dirs_out, perm, group_of, ws, stream=None):
+    """PDDP grouping whose power iterations start from stored directions (dirs_in,
+    or None for the fixed start); final directions go to dirs_out (or None)."""
+    _expect(desc, q=q, perm=perm, group_of=group_of)
+    n = int(load().mcs_pddp_dirs_size(ctypes.byref(desc)))
+    for name, t in (("dirs_in", dirs_in), ("dirs_out", dirs_out)):
+        if t is not None and (t.dtype != torch.float32 or t.numel() * 4 != n):
+            raise ValueError(f"{name}: expected {n // 4} fp32 elements, got {t.numel()} {t.dtype}")
+    _check("mcs_group_pddp_warm", load().mcs_group_pddp_warm(ctypes.byref(desc), _ptr(q), _ptr(dirs_in), _ptr(dirs_out),
+                                                             _ptr(perm), _ptr(group_of), _ptr(ws), ws.numel(),
+                                                             _stream(stream)))
 
 
 def mcs_dense_attn(desc, q, k, v, o, lse, stream=None):

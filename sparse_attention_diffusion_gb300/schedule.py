@@ -44,9 +44,16 @@ class Schedule:
 
 
 class MetaCacheLayer:
-    """One attention layer with its caller-owned meta-cache buffers."""
+    """One attention layer with its caller-owned meta-cache buffers.
 
-    def __init__(self, desc: mcs.mcs_desc, K: int, dtype, device):
+    warm_iters: None groups every anchor from the fixed start (desc.pddp_iters
+    power iterations); an integer keeps the grouping's per-node directions
+    between anchors, so that every anchor after the first starts each node from
+    the previous anchor's direction and runs warm_iters iterations ("fast PDDP",
+    the amortised grouping). `masses` collects each anchor's mean captured
+    attention mass (untimed), the quality measure of the grouping."""
+
+    def __init__(self, desc: mcs.mcs_desc, K: int, dtype, device, warm_iters=None):
         self.desc, self.K = desc, K
         self.cache = mcs.alloc_cache(desc, K, dtype, device=device)
         self.ws = mcs.workspace(desc, K, device=device)
@@ -54,6 +61,22 @@ class MetaCacheLayer:
         self.o_dense = torch.empty(shape, dtype=dtype, device=device)
         self.lse = torch.empty((desc.B, desc.H, desc.N), dtype=torch.float32, device=device)
         self.out = torch.empty(shape, dtype=dtype, device=device)
+        self.warm_iters = warm_iters
+        self.masses = []
+        self._anchors = 0
+        if warm_iters is not None:
+            self.dirs = mcs.pddp_dirs(desc, device=device)
+            self.desc_warm = mcs.make_desc(desc.B, desc.H, desc.N, desc.d, desc.C, dtype, desc.scale, warm_iters)
+
+    def group(self, q):
+        c = self.cache
+        if self.warm_iters is None:
+            mcs.mcs_group_pddp(self.desc, q, c["perm"], c["group_of"], self.ws)
+        elif self._anchors == 0:
+            mcs.mcs_group_pddp_warm(self.desc, q, None, self.dirs, c["perm"], c["group_of"], self.ws)
+        else:
+            mcs.mcs_group_pddp_warm(self.desc_warm, q, self.dirs, self.dirs, c["perm"], c["group_of"], self.ws)
+        self._anchors += 1
 
     def dense(self, q, k, v):
         mcs.mcs_dense_attn(self.desc, q, k, v, self.o_dense, self.lse)
@@ -62,13 +85,18 @@ class MetaCacheLayer:
     def anchor(self, q, k, v, timer=None):
         c = self.cache
         t = timer or (lambda name, fn: fn())
-        t("pddp", lambda: mcs.mcs_group_pddp(self.desc, q, c["perm"], c["group_of"], self.ws))
+        t("pddp", lambda: self.group(q))
         t("dense", lambda: mcs.mcs_dense_attn(self.desc, q, k, v, self.o_dense, self.lse))
         t("select", lambda: mcs.mcs_anchor_select(self.desc, q, k, c["perm"], self.lse, self.K, c["idx"], c["mass"],
                                                   self.ws))
         t("anchor_residual", lambda: mcs.mcs_anchor_residual(self.desc, q, k, v, c["perm"], c["idx"], self.K,
                                                              self.o_dense, c["residual"]))
         return self.o_dense
+
+    def after_step(self, kind, q):
+        """Untimed work after a step: the anchor's mean captured mass."""
+        if kind == "anchor":
+            self.masses.append(float(self.cache["mass"].float().mean()))
 
     def reuse(self, q, k, v):
         c = self.cache
@@ -103,6 +131,8 @@ def run(layer: MetaCacheLayer, sched: Schedule, inputs, advance, on_output=None)
         else:
             out = layer.reuse(q, k, v)
         b0.record(stream)
+        if hasattr(layer, "after_step"):
+            layer.after_step(kind, q)
         if on_output is not None:
             on_output(t, kind, out)
         recs.append((kind, a0, b0, ev))

@@ -156,6 +156,51 @@ def test_pddp_hand_worked_odd_split():
     assert group_of.tolist() == [int(t) for t in kv["group_of"].split()]
 
 
+def test_pddp_hand_worked_warm_start():
+    """Stored start directions per tree node (level-by-level slots) with 0 power
+    iterations: the right node is then cut along x instead of its own principal
+    direction. Hand-worked in tests/golden/pddp_odd_split.txt."""
+    kv, pts = _golden_kv("pddp_odd_split.txt")
+    C = int(kv["C"])
+    x = np.zeros((len(pts), 2))
+    for i, a, b in pts:
+        x[i] = (a, b)
+    dirs = np.array([[float(t) for t in row.split()] for row in kv["warm_dirs"].split(";")])
+    perm, _ = orc.pddp_groups(x, len(pts), C, iters=int(kv["warm_iters"]), v_init=dirs)
+    assert perm.tolist() == [int(t) for t in kv["warm_perm"].split()]
+
+
+@pytest.mark.parametrize("N,C,d", [(1000, 64, 16), (700, 128, 8)])
+def test_pddp_warm_start_from_own_directions_reproduces_groups(N, C, d):
+    """Directions written by one grouping, fed back as start vectors with zero
+    iterations, give back the same groups (every node reads its own slot); the
+    default start equals a table of 1/sqrt(d) rows."""
+    x = _rng(N + d).standard_normal((N, d)) * np.linspace(3, 1, d)
+    G = -(-N // C)
+    xp = np.zeros((G * C, d))
+    xp[:N] = x
+    L = int(math.ceil(math.log2(G))) if G > 1 else 0
+    dirs = np.full(((1 << L) - 1, d), np.nan)
+    perm, _ = orc.pddp_groups(xp, N, C, iters=20, v_out=dirs)
+    perm0, _ = orc.pddp_groups(xp, N, C, iters=0, v_init=dirs)
+    assert np.array_equal(perm0, perm)
+    ones = np.full(((1 << L) - 1, d), 1 / math.sqrt(d))
+    perm1, _ = orc.pddp_groups(xp, N, C, iters=7, v_init=ones)
+    assert np.array_equal(perm1, orc.pddp_groups(xp, N, C, iters=7)[0])
+
+
+def test_principal_direction_warm_start_converges_to_eigh():
+    rng = _rng(17)
+    d = 12
+    basis, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    x = rng.standard_normal((3000, d)) * np.r_[3.0, np.linspace(1.5, 0.5, d - 1)] @ basis.T
+    xc = x - x.mean(axis=0)
+    v0 = rng.standard_normal(d)
+    v = orc.principal_direction(xc, iters=60, v0=v0 / np.linalg.norm(v0))
+    U = np.linalg.eigh(xc.T @ xc)[1]
+    assert abs(abs(v @ U[:, -1]) - 1.0) < 1e-10
+
+
 def test_pddp_hand_worked_pads_excluded():
     """Pads (zero rows at ids >= N) enter neither the node mean nor its covariance:
     with them, the x axis would win and a different real token would share the pad
