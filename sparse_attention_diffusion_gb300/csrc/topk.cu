@@ -1,11 +1,19 @@
 // Exact per-group top-K over the pass-2 score rows [MC-Sparse summary: anchor
 // two-pass paragraph: keep the K keys with the largest summed attention weight].
-// One CTA per row: an 8-bit-digit radix select finds the K-th largest score
-// (scores are non-negative fp32, so their bit patterns order like the values),
-// then an ordered compaction (contiguous slice per warp, one scan over the
-// warps) writes every key above it plus the lowest-index keys equal to it,
-// which gives ascending indices and the ties-to-lower-index rule at once. The
-// captured mass is summed in a fixed order.
+// One CTA per row. The K-th largest score is found by a radix
+// select on the scores' bit patterns (scores are non-negative fp32, so their
+// bit patterns order like the values), then an ordered compaction (contiguous
+// slice per warp, one scan over the warps) writes every key above it plus the
+// lowest-index keys equal to it, which gives ascending indices and the
+// ties-to-lower-index rule at once. The captured mass is summed in a fixed order.
+//
+// The select reads the row twice: pass A histograms the top 12 bits of every
+// score (4,096 bins in shared memory); pass B reads the row again and keeps the
+// scores of the K-th score's bin, whose count pass A gives, in shared memory
+// (up to kCap of them), where the remaining 20 bits are resolved (12, then 8).
+// A bin holding more than kCap scores is resolved by two more passes over the
+// row instead. With the compaction that makes three row reads in the common
+// case. Rows whose length is a multiple of 4 are read 16 bytes per load.
 #include "block_scan.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -16,66 +24,224 @@ namespace {
 
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kLoads = 8;  // independent row loads in flight per thread
+constexpr int kLoads = 8;       // independent 4-byte row loads in flight per thread (compaction)
+constexpr int kVecLoads = 2;    // independent 16-byte row loads in flight per thread (passes A, B)
+constexpr int kBinsA = 4096;    // pass A digit: bits 31..20
+constexpr int kCap = 8192;      // scores of the K-th bin kept in shared memory
+constexpr int kSmemBytes = kBinsA * 4 + kCap * 4;
 
+// Finds, over kBins bins ordered from the highest down, the bin b with
+// (elements in bins above b) < remaining <= that count + hist[b]. kBins is a
+// multiple of 1024; every thread of the block calls it. Writes the count above
+// b to *before and returns b (-1 if remaining exceeds the total).
+template <int kBins>
+__device__ __forceinline__ int block_find_digit_desc(const uint32_t* hist, uint32_t remaining, uint32_t* before,
+                                                     uint32_t* warp_tot, int* sh_bin, uint32_t* sh_before) {
+  constexpr int nbins = kBins, per = kBins / kTopkThreads;  // bins per thread, highest bins to thread 0
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t c[per];
+  uint32_t tot = 0;
+#pragma unroll
+  for (int i = 0; i < per; ++i) {
+    c[i] = hist[nbins - 1 - (tid * per + i)];
+    tot += c[i];
+  }
+  uint32_t incl = tot;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  if (tid == 0) *sh_bin = -1;
+  __syncthreads();
+  uint32_t run = incl - tot;
+  for (int w = 0; w < warp; ++w) run += warp_tot[w];
+#pragma unroll
+  for (int i = 0; i < per; ++i) {
+    if (run < remaining && remaining <= run + c[i]) {  // exactly one thread matches (when remaining <= total)
+      *sh_bin = nbins - 1 - (tid * per + i);
+      *sh_before = run;
+    }
+    run += c[i];
+  }
+  __syncthreads();
+  *before = *sh_before;
+  return *sh_bin;
+}
+
+template <bool kVec>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) {
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t sh_prefix, sh_remaining;
+  extern __shared__ uint32_t dyn[];
+  uint32_t* hist = dyn;            // [kBinsA]
+  uint32_t* cand = dyn + kBinsA;   // [kCap]
+  __shared__ uint32_t warp_tot[kTopkWarps];
   __shared__ int wgt[kTopkWarps], weq[kTopkWarps];
   __shared__ float warp_sum[kTopkWarps];
+  __shared__ int sh_bin;
+  __shared__ uint32_t sh_before, sh_ncand;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x;
   const int grow = p.row0 + row;
   const float* S = p.scores + size_t(row) * p.N;
   const uint32_t* U = reinterpret_cast<const uint32_t*>(S);
+  const uint4* U4 = reinterpret_cast<const uint4*>(S);
+  const int N4 = p.N / 4;
   const uint32_t lanes_below = (1u << lane) - 1u;
 
-  // Radix select, four 8-bit digits from the top. The block walks the row in
-  // chunks of 1024 so every warp stays converged; lanes of a warp that hit the
-  // same bin add their count with one shared-memory atomic (score exponents
-  // cluster, so a per-element atomic would serialise on a few bins).
-  uint32_t prefix = 0, mask = 0, remaining = uint32_t(p.K);
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
-    __syncthreads();
-    // kLoads chunks per step: their loads are issued together (the row does not
-    // fit in L1, so each is an L2 round trip)
-    for (int c0 = 0; c0 < p.N; c0 += kLoads * kTopkThreads) {
-      uint32_t u4[kLoads];
+  // ---- pass A: histogram of bits 31..20 over the whole row
+  for (int i = tid; i < kBinsA; i += kTopkThreads) hist[i] = 0;
+  __syncthreads();
+  if (kVec) {
+    for (int c0 = 0; c0 < N4; c0 += kVecLoads * kTopkThreads) {
+      uint4 v[kVecLoads];
 #pragma unroll
-      for (int k = 0; k < kLoads; ++k) {
+      for (int k = 0; k < kVecLoads; ++k) {
         const int j = c0 + k * kTopkThreads + tid;
-        u4[k] = j < p.N ? __ldg(U + j) : 0u;
+        v[k] = j < N4 ? __ldg(U4 + j) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int k = 0; k < kLoads; ++k) {
-        const int j = c0 + k * kTopkThreads + tid;
-        const bool cand = j < p.N && (u4[k] & mask) == prefix;
-        const unsigned act = __ballot_sync(0xffffffffu, cand);
-        if (cand) {
-          const uint32_t bin = (u4[k] >> shift) & 255u;
-          const unsigned peers = __match_any_sync(act, bin);
-          if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], uint32_t(__popc(peers)));
+      for (int k = 0; k < kVecLoads; ++k) {
+        if (c0 + k * kTopkThreads + tid < N4) {
+          atomicAdd(&hist[v[k].x >> 20], 1u);
+          atomicAdd(&hist[v[k].y >> 20], 1u);
+          atomicAdd(&hist[v[k].z >> 20], 1u);
+          atomicAdd(&hist[v[k].w >> 20], 1u);
         }
       }
     }
+  } else {
+    for (int c0 = 0; c0 < p.N; c0 += kLoads * kTopkThreads) {
+      uint32_t u[kLoads];
+#pragma unroll
+      for (int k = 0; k < kLoads; ++k) {
+        const int j = c0 + k * kTopkThreads + tid;
+        u[k] = j < p.N ? __ldg(U + j) : 0u;
+      }
+#pragma unroll
+      for (int k = 0; k < kLoads; ++k)
+        if (c0 + k * kTopkThreads + tid < p.N) atomicAdd(&hist[u[k] >> 20], 1u);
+    }
+  }
+  __syncthreads();
+  uint32_t before;
+  const int bA = block_find_digit_desc<kBinsA>(hist, uint32_t(p.K), &before, warp_tot, &sh_bin, &sh_before);
+  uint32_t remaining = uint32_t(p.K) - before;  // how many of bin bA's scores are kept
+  const uint32_t nA = bA >= 0 ? hist[bA] : 0u;
+  uint32_t prefix = uint32_t(bA < 0 ? 0 : bA) << 20, mask = 0xFFF00000u;
+  __syncthreads();
+
+  if (nA <= uint32_t(kCap)) {
+    // ---- pass B: the scores of bin bA into shared memory, resolved there
+    if (tid == 0) sh_ncand = 0;
     __syncthreads();
-    if (warp == 0) {
-      uint32_t before;
-      const int b = warp_find_digit(hist, remaining, /*descending=*/true, &before);
-      if (lane == 0) {
-        sh_prefix = prefix | (uint32_t(b < 0 ? 0 : b) << shift);
-        sh_remaining = remaining - before;
+    auto keep = [&](uint32_t u) {
+      if ((u & mask) == prefix) cand[atomicAdd(&sh_ncand, 1u)] = u;
+    };
+    if (kVec) {
+      for (int c0 = 0; c0 < N4; c0 += kVecLoads * kTopkThreads) {
+        uint4 v[kVecLoads];
+#pragma unroll
+        for (int k = 0; k < kVecLoads; ++k) {
+          const int j = c0 + k * kTopkThreads + tid;
+          v[k] = j < N4 ? __ldg(U4 + j) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int k = 0; k < kVecLoads; ++k) {
+          if (c0 + k * kTopkThreads + tid < N4) {
+            keep(v[k].x);
+            keep(v[k].y);
+            keep(v[k].z);
+            keep(v[k].w);
+          }
+        }
+      }
+    } else {
+      for (int c0 = 0; c0 < p.N; c0 += kLoads * kTopkThreads) {
+        uint32_t u[kLoads];
+#pragma unroll
+        for (int k = 0; k < kLoads; ++k) {
+          const int j = c0 + k * kTopkThreads + tid;
+          u[k] = j < p.N ? __ldg(U + j) : 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < kLoads; ++k)
+          if (c0 + k * kTopkThreads + tid < p.N) keep(u[k]);
       }
     }
     __syncthreads();
-    prefix = sh_prefix;
-    remaining = sh_remaining;
-    mask |= 0xFFu << shift;
+    const int nc = int(sh_ncand);  // == nA
+    // bits 19..8 (4,096 bins), then bits 7..0 (256 bins), over the kept scores
+    for (int i = tid; i < kBinsA; i += kTopkThreads) hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < nc; i += kTopkThreads) atomicAdd(&hist[(cand[i] >> 8) & 0xFFFu], 1u);
+    __syncthreads();
+    const int bB = block_find_digit_desc<kBinsA>(hist, remaining, &before, warp_tot, &sh_bin, &sh_before);
+    remaining -= before;
+    prefix |= uint32_t(bB < 0 ? 0 : bB) << 8;
+    mask |= 0xFFF00u;
+    __syncthreads();
+    for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < nc; i += kTopkThreads)
+      if ((cand[i] & mask) == prefix) atomicAdd(&hist[cand[i] & 0xFFu], 1u);
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t b4;
+      const int b = warp_find_digit(hist, remaining, /*descending=*/true, &b4);
+      if (lane == 0) {
+        sh_bin = b < 0 ? 0 : b;
+        sh_before = b4;
+      }
+    }
+    __syncthreads();
+    prefix |= uint32_t(sh_bin);
+    remaining -= sh_before;
+  } else {
+    // ---- a crowded bin: bits 19..8 and 7..0 by two more passes over the row
+    for (int pass = 0; pass < 2; ++pass) {
+      const int shift = pass == 0 ? 8 : 0;
+      const uint32_t dmask = pass == 0 ? 0xFFFu : 0xFFu;
+      const int nbins = pass == 0 ? kBinsA : 256;
+      for (int i = tid; i < nbins; i += kTopkThreads) hist[i] = 0;
+      __syncthreads();
+      for (int c0 = 0; c0 < p.N; c0 += kLoads * kTopkThreads) {
+        uint32_t u[kLoads];
+#pragma unroll
+        for (int k = 0; k < kLoads; ++k) {
+          const int j = c0 + k * kTopkThreads + tid;
+          u[k] = j < p.N ? __ldg(U + j) : 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < kLoads; ++k)
+          if (c0 + k * kTopkThreads + tid < p.N && (u[k] & mask) == prefix)
+            atomicAdd(&hist[(u[k] >> shift) & dmask], 1u);
+      }
+      __syncthreads();
+      int b;
+      if (pass == 0) {
+        b = block_find_digit_desc<kBinsA>(hist, remaining, &before, warp_tot, &sh_bin, &sh_before);
+      } else {
+        if (warp == 0) {
+          uint32_t b4;
+          const int bb = warp_find_digit(hist, remaining, /*descending=*/true, &b4);
+          if (lane == 0) {
+            sh_bin = bb;
+            sh_before = b4;
+          }
+        }
+        __syncthreads();
+        b = sh_bin;
+        before = sh_before;
+      }
+      remaining -= before;
+      prefix |= uint32_t(b < 0 ? 0 : b) << shift;
+      mask |= dmask << shift;
+      __syncthreads();
+    }
   }
-  const uint32_t thr = prefix;                 // bit pattern of the K-th largest score
-  const int need_eq = int(remaining);          // how many scores equal to it are kept (lowest indices)
+  const uint32_t thr = prefix;            // bit pattern of the K-th largest score
+  const int need_eq = int(remaining);     // how many scores equal to it are kept (lowest indices)
 
   // Ordered compaction: warp w owns the contiguous slice [lo, hi) of the row.
   // Counting pass, one exclusive scan over the warps' counts, then each warp
@@ -166,13 +332,24 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   if (tid == 0 && gt_all + min(eq_all, need_eq) != p.K) raise_status(p.status, kStatusBounds);
 }
 
+template <bool kVec>
+cudaError_t launch_topk(const TopkParams& p, int nrows, cudaStream_t stream) {
+  auto kern = topk_kernel<kVec>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<nrows, kTopkThreads, kSmemBytes, stream>>>(p);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t topk_rows(const TopkParams& p, int nrows, cudaStream_t stream) {
   if (nrows <= 0) return cudaSuccess;
-  topk_kernel<<<nrows, kTopkThreads, 0, stream>>>(p);
-  note_launches(1);
-  return cudaGetLastError();
+  // 16-byte loads need every row to start on a 16-byte boundary (N % 4 == 0;
+  // the score rows start at a 256-byte-aligned base)
+  if (p.N % 4 == 0 && (reinterpret_cast<uintptr_t>(p.scores) & 15u) == 0) return launch_topk<true>(p, nrows, stream);
+  return launch_topk<false>(p, nrows, stream);
 }
 
 }  // namespace mcs
