@@ -23,8 +23,7 @@
 //                                 row, each copying one chunk of every 128-byte
 //                                 half, so a thread holds 4 row ids per tile;
 //   warpgroup 4 (warp 16)         tensor-memory allocation and the MMA
-//                                 schedule, run by the whole warp with lane 0
-//                                 issuing (warps 17-19 idle).
+//                                 schedule, run by lane 0 (warps 17-19 idle).
 // The gather warps never wait for their own copies: each thread ends a tile's
 // key (value) copies with an asynchronous arrive on the stage's full barrier,
 // which completes when every thread's rows have landed; the MMA thread then
@@ -288,13 +287,13 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegMma));
     // ------------------------------------------------------------ MMA issuer (warp 16)
-    // The whole warp runs the schedule, so every operand is warp-uniform (barrier
-    // tests are voted); lane 0 issues the MMAs and the commits.
-    if (warp == kMmaWarp) {
-      const bool leader = lane == 0;
+    // Lane 0 runs the schedule alone: its waits, MMAs and commits (the other lanes
+    // go straight to the final barrier). Measured 2.4 % faster at the 720p layer
+    // than the whole warp computing the operands with lane 0 issuing.
+    if (warp == kMmaWarp && lane == 0) {
       constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
-      bool ok = warp_all(mbar_wait(q_full, 0, st));
+      bool ok = mbar_wait(q_full, 0, st);
       bool issued = false;
       if (ok) {
         fence_proxy_async_smem();  // rows written by the gather warps' cp.async copies
@@ -307,23 +306,23 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
       // that tells the softmax S_{j+2} is done also covers that PV (O is stable
       // when S_{j+2} is seen). The waits are blocking (bounded) waits.
       auto issue_s = [&](int j) -> bool {
-        if (!warp_all(mbar_wait(k_full + j % SK, uint32_t(j / SK) & 1, st))) return false;
+        if (!mbar_wait(k_full + j % SK, uint32_t(j / SK) & 1, st)) return false;
         fence_proxy_async_smem();  // key rows landed by cp.async, read by the tensor core
         tc_fence_after();
         const uint32_t klo = desc_lo_kmajor(sbase + L::kK + (j % SK) * L::kTile);
         const uint32_t tS = tmem + uint32_t((j & 1) * 128);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          tc_mma_ss_lo_if(leader, tS, qlo + kstep_kmajor(ks), klo + kstep_kmajor(ks), kIdescQK, ks > 0 ? 1u : 0u);
-        tc_commit_if(leader, s_full + (j & 1));
-        tc_commit_if(leader, k_empty + j % SK);
+          tc_mma_ss_lo(tS, qlo + kstep_kmajor(ks), klo + kstep_kmajor(ks), kIdescQK, ks > 0 ? 1u : 0u);
+        tc_commit(s_full + (j & 1));
+        tc_commit(k_empty + j % SK);
         issued = true;
         return true;
       };
       auto issue_pv = [&](int j) -> bool {
         // P_j written by warpgroup j%2 and the value rows in
-        if (!warp_all(mbar_wait(p_full + (j & 1), uint32_t(j >> 1) & 1, st) &&
-                      mbar_wait(v_full + j % SV, uint32_t(j / SV) & 1, st)))
+        if (!(mbar_wait(p_full + (j & 1), uint32_t(j >> 1) & 1, st) &&
+              mbar_wait(v_full + j % SV, uint32_t(j / SV) & 1, st)))
           return false;
         fence_proxy_async_smem();  // value rows landed by cp.async
         tc_fence_after();
@@ -331,8 +330,8 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
         const uint32_t tP = tmem + uint32_t((j & 1) * 128), tO = tmem + L::kColO + uint32_t((j & 1) * D);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          tc_mma_ts_lo_if(leader, tO, tP + ks * 8, vlo + kstep_mnmajor(ks), kIdescPV, (j >= 2 || ks > 0) ? 1u : 0u);
-        tc_commit_if(leader, v_empty + j % SV);
+          tc_mma_ts_lo(tO, tP + ks * 8, vlo + kstep_mnmajor(ks), kIdescPV, (j >= 2 || ks > 0) ? 1u : 0u);
+        tc_commit(v_empty + j % SV);
         return true;
       };
       if (ok) ok = issue_s(0);
@@ -341,11 +340,11 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
         ok = issue_pv(j);
         if (ok && j + 2 < T) ok = issue_s(j + 2);
       }
-      if (ok) tc_commit_if(leader, o_done);
+      if (ok) tc_commit(o_done);
       if (!ok) {
-        if (leader) raise_status(st, kStatusTimeout);
+        raise_status(st, kStatusTimeout);
         if (issued) {
-          tc_commit_if(leader, drain);
+          tc_commit(drain);
           mbar_wait(drain, 0, st);
         }
       }
