@@ -458,7 +458,9 @@ def sweep_table(dev, peak_tflops):
         t = table.setdefault(f"d{r['d']}-c{r['C']}", {"density": [], "K": [], "sparse_ms": [], "tflops": [],
                                                        "frac": [], "speedup_vs_dense": [],
                                                        "dense_ms": r["dense_ms"]})
-        for key in ("density", "K", "sparse_ms", "tflops", "frac", "speedup_vs_dense"):
+        for key in ("density", "K"):
+            t[key].append(r[key])
+        for key in ("sparse_ms", "tflops", "frac", "speedup_vs_dense"):
             t[key].append(_r(r[key]))
     return {"workload": synth.SWEEP.name, "B": 1, "H": synth.SWEEP.H, "N": synth.SWEEP.N,
             "peak_kind": "measured sustained bf16", "by_shape": table}
