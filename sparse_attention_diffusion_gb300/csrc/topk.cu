@@ -7,13 +7,18 @@
 // lowest-index keys equal to it, which gives ascending indices and the
 // ties-to-lower-index rule at once. The captured mass is summed in a fixed order.
 //
-// The select reads the row twice: pass A histograms the top 12 bits of every
-// score (4,096 bins in shared memory); pass B reads the row again and keeps the
-// scores of the K-th score's bin, whose count pass A gives, in shared memory
-// (up to kCap of them), where the remaining 20 bits are resolved (12, then 8).
-// A bin holding more than kCap scores is resolved by two more passes over the
-// row instead. With the compaction that makes three row reads in the common
-// case. Rows whose length is a multiple of 4 are read 16 bytes per load.
+// Three passes over the row in the common case. Pass A histograms the top 12
+// bits of every score (4,096 bins in shared memory). Pass B walks each warp's
+// contiguous slice of the row: it counts the scores in bins above the K-th
+// score's bin (all kept) and keeps that bin's scores (up to kCap of them, with
+// their positions) in shared memory, where the remaining 20 bits are resolved
+// (12, then 8) and each warp's counts of kept and equal scores are completed
+// from the candidates' positions. The compaction pass then writes each warp's
+// slice, a lane taking a run of 8 consecutive scores (two 16-byte loads) and
+// one warp scan per 256 scores placing the lanes' kept positions. A bin holding
+// more than kCap scores is resolved by two more passes over the row, and the
+// slices are then counted by one more. Rows whose length is not a multiple of 4
+// are read 4 bytes per load.
 #include "block_scan.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -24,11 +29,11 @@ namespace {
 
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kLoads = 8;       // independent 4-byte row loads in flight per thread (compaction)
-constexpr int kVecLoads = 2;    // independent 16-byte row loads in flight per thread (passes A, B)
+constexpr int kLoads = 8;       // independent 4-byte row loads in flight per thread (strided passes)
+constexpr int kVecLoads = 2;    // independent 16-byte row loads in flight per thread (pass A)
 constexpr int kBinsA = 4096;    // pass A digit: bits 31..20
 constexpr int kCap = 8192;      // scores of the K-th bin kept in shared memory
-constexpr int kSmemBytes = kBinsA * 4 + kCap * 4;
+constexpr int kSmemBytes = kBinsA * 4 + kCap * 8;  // histogram, candidate scores and positions
 
 // Finds, over kBins bins ordered from the highest down, the bin b with
 // (elements in bins above b) < remaining <= that count + hist[b]. kBins is a
@@ -70,11 +75,49 @@ __device__ __forceinline__ int block_find_digit_desc(const uint32_t* hist, uint3
   return *sh_bin;
 }
 
+// Loads the V consecutive scores of a row starting at j0 (a multiple of V),
+// zeros from hi on: two 16-byte loads (kVec: hi is then a multiple of 4) or V
+// independent 4-byte loads.
+template <int V, bool kVec>
+__device__ __forceinline__ void load_run(const uint32_t* U, int j0, int hi, uint32_t (&u)[V]) {
+  if constexpr (kVec) {
+    static_assert(V % 4 == 0, "runs of whole 16-byte vectors");
+#pragma unroll
+    for (int h = 0; h < V / 4; ++h) {
+      const int j = j0 + 4 * h;
+      const uint4 x = j < hi ? __ldg(reinterpret_cast<const uint4*>(U + j)) : make_uint4(0, 0, 0, 0);
+      u[4 * h] = x.x;
+      u[4 * h + 1] = x.y;
+      u[4 * h + 2] = x.z;
+      u[4 * h + 3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int t = 0; t < V; ++t) u[t] = j0 + t < hi ? __ldg(U + j0 + t) : 0u;
+  }
+}
+
+// Exclusive prefix sum of v over the warp's lanes; *total gets the warp's sum.
+__device__ __forceinline__ int warp_excl_sum(int v, int lane, int* total) {
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  *total = __shfl_sync(0xffffffffu, incl, 31);
+  return incl - v;
+}
+
 template <bool kVec>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) {
+  // a lane's run of consecutive scores in the slice passes: 8 (two 16-byte
+  // loads) when rows allow 16-byte loads, else 4
+  constexpr int V = kVec ? 8 : 4;
   extern __shared__ uint32_t dyn[];
-  uint32_t* hist = dyn;            // [kBinsA]
-  uint32_t* cand = dyn + kBinsA;   // [kCap]
+  uint32_t* hist = dyn;                                        // [kBinsA]
+  uint32_t* cand = dyn + kBinsA;                               // [kCap] scores of bin bA
+  int32_t* cand_idx = reinterpret_cast<int32_t*>(cand + kCap);  // [kCap] their positions
   __shared__ uint32_t warp_tot[kTopkWarps];
   __shared__ int wgt[kTopkWarps], weq[kTopkWarps];
   __shared__ float warp_sum[kTopkWarps];
@@ -87,7 +130,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   const uint32_t* U = reinterpret_cast<const uint32_t*>(S);
   const uint4* U4 = reinterpret_cast<const uint4*>(S);
   const int N4 = p.N / 4;
-  const uint32_t lanes_below = (1u << lane) - 1u;
+  // warp w owns the contiguous slice [lo, hi) of the row in the slice passes
+  // (a multiple of 256 scores long, so runs never straddle two warps)
+  const int span = ((p.N + kTopkWarps - 1) / kTopkWarps + 255) & ~255;
+  const int lo = min(p.N, warp * span), hi = min(p.N, lo + span);
 
   // ---- pass A: histogram of bits 31..20 over the whole row
   for (int i = tid; i < kBinsA; i += kTopkThreads) hist[i] = 0;
@@ -132,45 +178,37 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   __syncthreads();
 
   if (nA <= uint32_t(kCap)) {
-    // ---- pass B: the scores of bin bA into shared memory, resolved there
+    // ---- pass B, over each warp's slice: count the scores in bins above bA
+    // (all kept) and keep bin bA's scores with their positions in shared memory
     if (tid == 0) sh_ncand = 0;
+    if (tid < kTopkWarps) weq[tid] = 0;
     __syncthreads();
-    auto keep = [&](uint32_t u) {
-      if ((u & mask) == prefix) cand[atomicAdd(&sh_ncand, 1u)] = u;
-    };
-    if (kVec) {
-      for (int c0 = 0; c0 < N4; c0 += kVecLoads * kTopkThreads) {
-        uint4 v[kVecLoads];
+    int above = 0;
+    for (int c = lo; c < hi; c += 32 * V) {
+      const int j0 = c + lane * V;
+      uint32_t u[V];
+      load_run<V, kVec>(U, j0, hi, u);
 #pragma unroll
-        for (int k = 0; k < kVecLoads; ++k) {
-          const int j = c0 + k * kTopkThreads + tid;
-          v[k] = j < N4 ? __ldg(U4 + j) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int k = 0; k < kVecLoads; ++k) {
-          if (c0 + k * kTopkThreads + tid < N4) {
-            keep(v[k].x);
-            keep(v[k].y);
-            keep(v[k].z);
-            keep(v[k].w);
+      for (int t = 0; t < V; ++t) {
+        const int b = int(u[t] >> 20);
+        if (j0 + t < hi) {
+          above += b > bA ? 1 : 0;
+          if (b == bA) {
+            const uint32_t slot = atomicAdd(&sh_ncand, 1u);
+            if (slot < uint32_t(kCap)) {
+              cand[slot] = u[t];
+              cand_idx[slot] = j0 + t;
+            }
           }
         }
       }
-    } else {
-      for (int c0 = 0; c0 < p.N; c0 += kLoads * kTopkThreads) {
-        uint32_t u[kLoads];
-#pragma unroll
-        for (int k = 0; k < kLoads; ++k) {
-          const int j = c0 + k * kTopkThreads + tid;
-          u[k] = j < p.N ? __ldg(U + j) : 0u;
-        }
-#pragma unroll
-        for (int k = 0; k < kLoads; ++k)
-          if (c0 + k * kTopkThreads + tid < p.N) keep(u[k]);
-      }
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) above += __shfl_xor_sync(0xffffffffu, above, off);
+    if (lane == 0) wgt[warp] = above;
     __syncthreads();
-    const int nc = int(sh_ncand);  // == nA
+    const int nc = int(min(sh_ncand, uint32_t(kCap)));  // == nA
+    if (tid == 0 && sh_ncand != nA) raise_status(p.status, kStatusBounds);
     // bits 19..8 (4,096 bins), then bits 7..0 (256 bins), over the kept scores
     for (int i = tid; i < kBinsA; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
@@ -197,6 +235,14 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     __syncthreads();
     prefix |= uint32_t(sh_bin);
     remaining -= sh_before;
+    // each warp's counts of kept (> threshold) and equal scores: its bin-bA
+    // candidates added to the scores above bin bA
+    for (int i = tid; i < nc; i += kTopkThreads) {
+      const int w = cand_idx[i] / span;
+      if (cand[i] > prefix) atomicAdd(&wgt[w], 1);
+      else if (cand[i] == prefix) atomicAdd(&weq[w], 1);
+    }
+    __syncthreads();
   } else {
     // ---- a crowded bin: bits 19..8 and 7..0 by two more passes over the row
     for (int pass = 0; pass < 2; ++pass) {
@@ -239,41 +285,38 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
       mask |= dmask << shift;
       __syncthreads();
     }
+    // each warp counts its slice's kept and equal scores
+    int cgt = 0, ceq = 0;
+    for (int c = lo; c < hi; c += 32 * V) {
+      const int j0 = c + lane * V;
+      uint32_t u[V];
+      load_run<V, kVec>(U, j0, hi, u);
+#pragma unroll
+      for (int t = 0; t < V; ++t) {
+        const bool v = j0 + t < hi;
+        cgt += (v && u[t] > prefix) ? 1 : 0;
+        ceq += (v && u[t] == prefix) ? 1 : 0;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      cgt += __shfl_xor_sync(0xffffffffu, cgt, off);
+      ceq += __shfl_xor_sync(0xffffffffu, ceq, off);
+    }
+    if (lane == 0) {
+      wgt[warp] = cgt;
+      weq[warp] = ceq;
+    }
+    __syncthreads();
   }
   const uint32_t thr = prefix;            // bit pattern of the K-th largest score
   const int need_eq = int(remaining);     // how many scores equal to it are kept (lowest indices)
 
-  // Ordered compaction: warp w owns the contiguous slice [lo, hi) of the row.
-  // Counting pass, one exclusive scan over the warps' counts, then each warp
-  // writes its selected ids in index order with ballots (ties to the lower
-  // index: a warp keeps the first equal scores that the warps before it left).
-  const int span = ((p.N + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
-  const int lo = min(p.N, warp * span), hi = min(p.N, lo + span);
-  int cgt = 0, ceq = 0;
-  for (int c = lo; c < hi; c += kLoads * 32) {
-    uint32_t u4[kLoads];
-#pragma unroll
-    for (int k = 0; k < kLoads; ++k) {
-      const int j = c + k * 32 + lane;
-      u4[k] = j < hi ? __ldg(U + j) : 0u;
-    }
-#pragma unroll
-    for (int k = 0; k < kLoads; ++k) {
-      const bool v = c + k * 32 + lane < hi;
-      cgt += (v && u4[k] > thr) ? 1 : 0;
-      ceq += (v && u4[k] == thr) ? 1 : 0;
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    cgt += __shfl_xor_sync(0xffffffffu, cgt, off);
-    ceq += __shfl_xor_sync(0xffffffffu, ceq, off);
-  }
-  if (lane == 0) {
-    wgt[warp] = cgt;
-    weq[warp] = ceq;
-  }
-  __syncthreads();
+  // Ordered compaction over the warps' slices: one scan over the warps' counts
+  // gives each warp its first output position; a warp then writes its kept
+  // positions in index order, a lane taking a run of V consecutive scores and
+  // one warp scan placing the runs (ties to the lower index: a warp keeps the
+  // first equal scores that the warps before it left).
   int gt_before = 0, eq_before = 0, gt_all = 0, eq_all = 0;
   for (int w = 0; w < kTopkWarps; ++w) {
     const int a = wgt[w], b = weq[w];
@@ -282,34 +325,48 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     gt_all += a;
     eq_all += b;
   }
-  const int take_eq = max(0, min(ceq, need_eq - eq_before));
+  const int take_eq = max(0, min(weq[warp], need_eq - eq_before));
   int out_pos = gt_before + min(eq_before, need_eq);
   int eq_seen = 0;
   float msum = 0.f;
   int32_t* out = p.idx + size_t(grow) * p.K;
-  for (int c = lo; c < hi; c += kLoads * 32) {
-    uint32_t u4[kLoads];
+  for (int c = lo; c < hi; c += 32 * V) {
+    const int j0 = c + lane * V;
+    uint32_t u[V];
+    load_run<V, kVec>(U, j0, hi, u);
+    bool sel[V];
+    int ns = 0, ne = 0;
 #pragma unroll
-    for (int k = 0; k < kLoads; ++k) {
-      const int j = c + k * 32 + lane;
-      u4[k] = j < hi ? __ldg(U + j) : 0u;
+    for (int t = 0; t < V; ++t) {
+      const bool v = j0 + t < hi;
+      sel[t] = v && u[t] > thr;
+      ne += (v && u[t] == thr) ? 1 : 0;
     }
+    if (__any_sync(0xffffffffu, ne > 0)) {  // equal scores: the first take_eq of the slice are kept
+      int ne_all;
+      int e = eq_seen + warp_excl_sum(ne, lane, &ne_all);
 #pragma unroll
-    for (int k = 0; k < kLoads; ++k) {  // chunks in index order
-      const int j = c + k * 32 + lane;
-      const bool v = j < hi;
-      const bool gt = v && u4[k] > thr, eq = v && u4[k] == thr;
-      const unsigned beq = __ballot_sync(0xffffffffu, eq);
-      const bool sel = gt || (eq && eq_seen + __popc(beq & lanes_below) < take_eq);
-      const unsigned bsel = __ballot_sync(0xffffffffu, sel);
-      const int pos = out_pos + __popc(bsel & lanes_below);
-      if (sel && pos < p.K) {
-        out[pos] = j;
-        msum += __uint_as_float(u4[k]);
+      for (int t = 0; t < V; ++t) {
+        if (j0 + t < hi && u[t] == thr) {
+          sel[t] = e < take_eq;
+          ++e;
+        }
       }
-      out_pos += __popc(bsel);
-      eq_seen += __popc(beq);
+      eq_seen += ne_all;
     }
+#pragma unroll
+    for (int t = 0; t < V; ++t) ns += sel[t] ? 1 : 0;
+    int ns_all;
+    int pos = out_pos + warp_excl_sum(ns, lane, &ns_all);
+#pragma unroll
+    for (int t = 0; t < V; ++t) {
+      if (sel[t]) {
+        if (pos < p.K) out[pos] = j0 + t;
+        msum += __uint_as_float(u[t]);
+        ++pos;
+      }
+    }
+    out_pos += ns_all;
   }
   if (p.mass != nullptr) {
     const int bh = grow / p.G, g = grow % p.G;
