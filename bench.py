@@ -23,7 +23,9 @@ the group-shared selection with the PDDP groups against contiguous tile groups
 (`--no-matched` skips it).
 It also times the reuse step with the meta-cache kept in pinned host memory
 through the cache ring (three layers' entries, the next one prefetched while
-the current one computes; `cache_ring`; `--no-ring` skips it).
+the current one computes; `cache_ring`; `--no-ring` skips it), and the reuse
+kernel on uniform random sorted key sets of the same size (`stress_random_idx`;
+`--no-stress` skips it).
 `--impl reference` times the float64 CPU oracle instead, on a bounded sample of
 groups, extrapolated to ms/layer.
 """
@@ -63,6 +65,8 @@ def parse():
     ap.add_argument("--no-schedule", action="store_true", help="skip the 118,800-token schedule (anchor overhead)")
     ap.add_argument("--no-sweep", action="store_true", help="skip the 65,536-token density/tile sweep")
     ap.add_argument("--no-ring", action="store_true", help="skip the host-resident meta-cache (cache ring) timing")
+    ap.add_argument("--no-stress", action="store_true",
+                    help="skip the reuse kernel on uniform random key sets (stress variant of the selected ones)")
     ap.add_argument("--no-matched", action="store_true", help="skip the PDDP-vs-contiguous group mass comparison")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the tiny fp32 layer and the 480p-shaped layer (1 anchor + reuse steps each)")
@@ -313,6 +317,44 @@ def cache_ring_timing(desc, K, q, k, v, cache, stream):
                 "note": "perm+idx+residual per layer in pinned host memory, two device slots; second pass over the layers timed"}
     finally:
         ring.close()
+
+
+def stress_random_indices(desc, K, q, k, v, cache, stream, peak, wl, reps=5, warm=3, seed=1234):
+    """The reuse kernel on the same layer with uniform random key sets instead of
+    the anchor's selection: per (head, group) K distinct keys drawn uniformly
+    (seeded), sorted ascending. The gathers then follow no locality of the
+    selected keys; the arithmetic is unchanged."""
+    import torch
+    from sparse_attention_diffusion_gb300 import mcs
+
+    idx = torch.empty_like(cache["idx"])
+    rows = idx.numel() // K
+    flat = idx.view(rows, K)
+    gen = torch.Generator(device=q.device)
+    gen.manual_seed(seed)
+    for r0 in range(0, rows, 1024):
+        r1 = min(rows, r0 + 1024)
+        u = torch.rand((r1 - r0, wl.N), generator=gen, device=q.device)
+        flat[r0:r1] = torch.sort(torch.topk(u, K, dim=1, sorted=False).indices.to(torch.int32), dim=1).values
+        del u
+    o = torch.empty_like(q)
+    f = lambda: mcs.mcs_sparse_attn_gather(desc, q, k, v, cache["perm"], idx, K, cache["residual"], o)
+    for _ in range(warm):
+        f()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        f()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    mcs.mcs_check_status()
+    ms = statistics.median(ts)
+    tf = flops_sparse(wl, K) / (ms * 1e-3) / 1e12
+    del idx, o
+    return {"what": "reuse kernel, uniform random sorted key sets (seeded), same layer and K",
+            "ms": ms, "tflops": tf, "frac": tf / peak, "calls_ms": [round(x, 3) for x in ts], "stat": f"median of {reps}"}
 
 
 def matched_density(desc, K, q, k, v, o_dense, cache, ws):
@@ -714,6 +756,8 @@ def run_mcs(args, wl, K):
         }
         if world == 1 and not args.no_matched:
             line["matched_density"] = matched_density(desc, K, q, k, v, o_dense, cache, ws)
+        if world == 1 and not args.no_stress:
+            line["stress_random_idx"] = stress_random_indices(desc, K, q2, k2, v2, cache, stream, pk["bf16_sus"], wl)
         if world == 1 and not args.no_ring:
             ring = cache_ring_timing(desc, K, q2, k2, v2, cache, stream)
             ring["resident_ms_per_layer"] = sparse_ms
@@ -759,6 +803,9 @@ def summary(line, wl):
     out[wl.name] = {"stages_ms": {k: _r(v) for k, v in line["stages_ms"].items()}, "sparse_tflops": _r(line["tflops"]),
                     "frac": _r(line["roofline"]["frac"], 3), "speedup": _r(line["speedup_vs_dense"], 3),
                     "cpu_ms": {"anchor": _r((cb.get("anchor") or {}).get("value")), "reuse": _r(cb.get("value"))}}
+    st = line.get("stress_random_idx")
+    if st:
+        out[wl.name]["random_idx"] = {"ms": _r(st["ms"]), "frac": _r(st["frac"], 3)}
     ao = line.get("anchor_overhead")
     if ao:
         out[ao["workload"]] = {rho: {"total_ms": _r(v["total_ms"]), "overhead_pts": _r(v["anchor_overhead_points"], 3),

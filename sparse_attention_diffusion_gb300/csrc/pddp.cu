@@ -300,11 +300,17 @@ __global__ void __launch_bounds__(256) cov_kernel(const T* __restrict__ x, const
 
 // 3b. node covariance (fixed-order sum of its chunks) and the power iterations.
 // kRaw: the chunks hold raw second moments (tensor-core path), so the node's
-// n mu mu^T is subtracted once here.
+// n mu mu^T is subtracted once here. The chunk sum keeps kEb elements of a
+// thread in registers so that their loads of one chunk are in flight together
+// (the sum over chunks stays in chunk order; a shallow node has dozens of
+// chunks, and one load at a time left the sum waiting on memory latency).
 template <typename A, int D, bool kRaw>
 __global__ void __launch_bounds__(256) power_kernel(Tables t, int level, int G, const A* pcov, A* node_v, int iters,
                                                     int max_chunks, const A* node_mu, const int* pcnt, float* dirs_out,
                                                     int slots) {
+  constexpr int kThreads = 256;
+  constexpr int kEb = 16;            // covariance elements per thread per round of the chunk sum
+  static_assert((D * D) % (kThreads * kEb) == 0, "shape");
   extern __shared__ uint8_t dyn[];
   A* cov = reinterpret_cast<A*>(dyn);  // [D][D]
   A* v = cov + D * D;                  // [D]
@@ -319,11 +325,23 @@ __global__ void __launch_bounds__(256) power_kernel(Tables t, int level, int G, 
   if (kRaw)
     for (int c = 0; c < nc; ++c) cnt += pcnt[size_t(bh) * max_chunks + c0 + c];
   __syncthreads();
-  for (int e = threadIdx.x; e < D * D; e += blockDim.x) {
-    A s = 0;
-    for (int c = 0; c < nc; ++c) s += pcov[(size_t(bh) * max_chunks + c0 + c) * D * D + e];
-    if (kRaw) s -= (A(cnt) * w[e / D]) * w[e % D];
-    cov[e] = s;
+  const A* pc = pcov + (size_t(bh) * max_chunks + c0) * D * D;
+  for (int e0 = threadIdx.x; e0 < D * D; e0 += kThreads * kEb) {
+    A acc[kEb];
+#pragma unroll
+    for (int i = 0; i < kEb; ++i) acc[i] = 0;
+    for (int c = 0; c < nc; ++c) {
+      const A* src = pc + size_t(c) * D * D + e0;
+#pragma unroll
+      for (int i = 0; i < kEb; ++i) acc[i] += src[i * kThreads];
+    }
+#pragma unroll
+    for (int i = 0; i < kEb; ++i) {
+      const int e = e0 + i * kThreads;
+      A s = acc[i];
+      if (kRaw) s -= (A(cnt) * w[e / D]) * w[e % D];
+      cov[e] = s;
+    }
   }
   __syncthreads();
   if (threadIdx.x < D) v[threadIdx.x] = node_v[(size_t(bh) * G + k) * D + threadIdx.x];
