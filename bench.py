@@ -446,7 +446,7 @@ def schedule_overhead(dev, peak_tflops, warm_iters=4):
     return out
 
 
-def sweep_table(dev, peak_tflops):
+def sweep_table(dev, peak_tflops, peak_texp=None):
     """The density/tile sweep layer (16 heads, N = 65,536, bf16) for d and C in
     {64, 128}: groups and dense attention once per (d, C), then for every density
     the anchor selection and the reuse-step sparse kernel, timed with CUDA events
@@ -489,23 +489,42 @@ def sweep_table(dev, peak_tflops):
             mcs.mcs_anchor_residual(desc, q, k, v, cache["perm"], idx, K, o_dense, cache["residual"])
             t = timed(lambda: mcs.mcs_sparse_attn_gather(desc, q, k, v, cache["perm"], idx, K, cache["residual"], o), 5)
             tf = 4.0 * wl0.B * wl0.H * wl0.N * K * d / (t * 1e-3) / 1e12
+            texp = wl0.B * wl0.H * wl0.N * K / (t * 1e-3) / 1e12   # kept (real query, key) exponentials
             rows.append({"d": d, "C": C, "density": float(rho), "K": K, "sparse_ms": t, "tflops": tf,
-                         "frac": tf / peak_tflops, "dense_ms": t_dense, "speedup_vs_dense": t_dense / t,
-                         "ideal_speedup": 1.0 / float(rho)})
+                         "frac": tf / peak_tflops, "exp_frac": (texp / peak_texp) if peak_texp else None,
+                         "dense_ms": t_dense, "speedup_vs_dense": t_dense / t, "ideal_speedup": 1.0 / float(rho)})
         mcs.mcs_check_status()
         del q, k, v, o_dense, lse, o, cache, ws
         torch.cuda.empty_cache()
     table = {}
     for r in rows:
         t = table.setdefault(f"d{r['d']}-c{r['C']}", {"density": [], "K": [], "sparse_ms": [], "tflops": [],
-                                                       "frac": [], "speedup_vs_dense": [],
+                                                       "frac": [], "exp_frac": [], "speedup_vs_dense": [],
                                                        "dense_ms": r["dense_ms"]})
         for key in ("density", "K"):
             t[key].append(r[key])
-        for key in ("sparse_ms", "tflops", "frac", "speedup_vs_dense"):
+        for key in ("sparse_ms", "tflops", "frac", "exp_frac", "speedup_vs_dense"):
             t[key].append(_r(r[key]))
     return {"workload": synth.SWEEP.name, "B": 1, "H": synth.SWEEP.H, "N": synth.SWEEP.N,
-            "peak_kind": "measured sustained bf16", "by_shape": table}
+            "peak_kind": "measured sustained bf16",
+            "exp_frac_of": "kept exponentials (B*H*N*K per launch) per second over the measured ex2 peak",
+            "by_shape": table}
+
+
+def exp_peak(dev, sm_max_mhz):
+    """Peak exponential rate (T exp/s): the library's ex2 diagnostic measures
+    exponentials per SM clock (one CTA per SM), scaled by the SM count and the
+    maximum SM clock."""
+    import torch
+
+    from sparse_attention_diffusion_gb300 import mcs
+
+    per_clk = mcs.ex2_per_clock_per_sm()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    return {"ex2_per_clk_sm": per_clk, "sms": sms, "sm_mhz": sm_max_mhz,
+            "peak_texp_s": per_clk * sms * sm_max_mhz * 1e6 / 1e12,
+            "how": "mcs_selftest_ex2_rate: 1,024 threads x 8 chains of ex2.approx.ftz.f32 per CTA, one CTA per SM, "
+                   "median over SMs of exponentials / clock64 cycles"}
 
 
 def fp32_alu_peak_tflops(sm_max_mhz):
@@ -764,8 +783,11 @@ def run_mcs(args, wl, K):
             line["cache_ring"] = ring
         if world == 1 and not args.no_schedule:
             line["anchor_overhead"] = schedule_overhead(dev, pk["bf16_sus"])
+        ep = exp_peak(dev, pk["sm_max_mhz"])
+        texp = wl.B * wl.H * wl.N * K / (sparse_ms * 1e-3) / 1e12
+        line["exp_unit"] = dict(ep, sparse_texp_s=texp, sparse_exp_frac=texp / ep["peak_texp_s"])
         if world == 1 and not args.no_sweep:
-            line["sweep"] = sweep_table(dev, pk["bf16_sus"])
+            line["sweep"] = sweep_table(dev, pk["bf16_sus"], ep["peak_texp_s"])
         if world == 1 and not args.no_configs:
             line["configs"] = {c.name: config_measure(c, dev, pk, n, cpu=not args.no_cpu_baseline)
                                for c, n in ((synth.TINY, 1), (synth.WAN13_480P, 4))}
@@ -820,7 +842,8 @@ def summary(line, wl):
                                for rho, v in ao.items() if isinstance(v, dict) and "total_ms" in v}
     sw = line.get("sweep")
     if sw:
-        out[sw["workload"]] = {shape: {"frac": t["frac"], "speedup": [_r(x, 3) for x in t["speedup_vs_dense"]]}
+        out[sw["workload"]] = {shape: {"frac": t["frac"], "exp_frac": t.get("exp_frac"),
+                                       "speedup": [_r(x, 3) for x in t["speedup_vs_dense"]]}
                                for shape, t in sw["by_shape"].items()}
     return out
 

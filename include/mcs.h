@@ -274,6 +274,16 @@ mcs_status mcs_selftest_tc_mma(const void *a, const void *b, float *d, int mode,
  * uint64 receiving the wait's duration in ns, or NULL. */
 mcs_status mcs_selftest_wait_timeout(uint64_t limit_ns, uint64_t *elapsed_ns, mcs_stream stream);
 
+/* Diagnostic (no counterpart in the method): the rate of the exponential unit as
+ * the attention softmax uses it (ex2.approx.ftz.f32), which bounds kernels with
+ * few FLOPs per exponential (d = 64 tiles, the pass-2 column sums). Launches
+ * nblocks (1 .. 65535; one per SM gives the whole GPU) CTAs of 1,024 threads, one
+ * per SM at a time, each thread running eight independent chains of `iters`
+ * (1 .. 2^24) exponentials. out: device uint64 [nblocks][2] receiving each CTA's
+ * duration in SM clock cycles and the number of exponentials it computed (their
+ * ratio is exponentials per clock per SM). Asynchronous on `stream`. */
+mcs_status mcs_selftest_ex2_rate(int iters, int nblocks, uint64_t *out, mcs_stream stream);
+
 /* Diagnostic (no counterpart in the method): gathers 128 rows of the bf16 matrix
  * src [nrows x 128] (row-major, device) with TMA 4-row gathers into the swizzled
  * shared-memory layout of the attention kernels and writes them back row-major:

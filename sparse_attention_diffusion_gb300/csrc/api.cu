@@ -554,6 +554,17 @@ mcs_status mcs_selftest_wait_timeout(uint64_t limit_ns, uint64_t* elapsed_ns, mc
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
+mcs_status mcs_selftest_ex2_rate(int iters, int nblocks, uint64_t* out, mcs_stream stream) {
+  if (iters < 1 || iters > (1 << 24) || nblocks < 1 || nblocks > 65535 || out == nullptr ||
+      (reinterpret_cast<uintptr_t>(out) & 7u) != 0)
+    return MCS_ERR_INVALID_ARG;
+  uint32_t* status = nullptr;
+  mcs_status st = device_state(&status, nullptr);
+  if (st != MCS_OK) return st;
+  return from_cuda(mcs::ex2_rate_probe(iters, nblocks, reinterpret_cast<unsigned long long*>(out),
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
 mcs_status mcs_selftest_tma_gather(const void* src, int nrows, const int32_t* rows, void* out, mcs_stream stream) {
   if (!aligned16(src) || !aligned16(rows) || !aligned16(out) || nrows < 1) return MCS_ERR_INVALID_ARG;
   uint32_t* status = nullptr;

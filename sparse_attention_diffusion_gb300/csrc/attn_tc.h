@@ -41,6 +41,7 @@ cudaError_t tc_colsum(int D, int C, const TcColsumParams& p, int nrows, cudaStre
 cudaError_t tma_gather_probe(const void* src, int nrows, const int* rows, void* out, uint32_t* status,
                              cudaStream_t stream);
 cudaError_t wait_timeout_probe(uint64_t limit_ns, unsigned long long* elapsed, uint32_t* status, cudaStream_t stream);
+cudaError_t ex2_rate_probe(int iters, int nblocks, unsigned long long* out, cudaStream_t stream);
 cudaError_t tc_probe(const void* a, const void* b, float* d, int mode, uint32_t lbo, uint32_t sbo, uint32_t* status,
                      cudaStream_t stream);
 

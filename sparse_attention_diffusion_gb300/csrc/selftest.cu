@@ -171,7 +171,43 @@ __global__ void __launch_bounds__(128, 1) wait_timeout_probe_kernel(uint64_t lim
   }
 }
 
+// Throughput of the exponential unit as the softmax uses it: every thread runs
+// eight independent chains of ex2.approx.ftz.f32 (x <- 2^-x stays in (0.5, 1]),
+// 32 warps per CTA; the dynamic shared memory it asks for (but does not use)
+// keeps one CTA per SM, so a CTA's clock64 span is its SM's time for the count.
+constexpr int kEx2Threads = 1024, kEx2Chains = 8;
+__global__ void __launch_bounds__(kEx2Threads, 1) ex2_rate_kernel(int iters, unsigned long long* out) {
+  float x[kEx2Chains];
+#pragma unroll
+  for (int k = 0; k < kEx2Chains; ++k) x[k] = 0.001f * float(threadIdx.x & 31) + 0.1f * float(k);
+  __syncthreads();
+  const long long t0 = clock64();
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int k = 0; k < kEx2Chains; ++k) x[k] = ex2_approx(-x[k]);
+  }
+  __syncthreads();
+  const long long t1 = clock64();
+  float acc = 0.f;
+#pragma unroll
+  for (int k = 0; k < kEx2Chains; ++k) acc += x[k];
+  if (threadIdx.x == 0) {
+    out[2 * blockIdx.x] = static_cast<unsigned long long>(t1 - t0);
+    out[2 * blockIdx.x + 1] = static_cast<unsigned long long>(kEx2Threads) * kEx2Chains * unsigned(iters);
+  }
+  if (acc < 0.f) out[2 * blockIdx.x + 1] = 0;  // never true; keeps the chains live
+}
+
 }  // namespace
+
+cudaError_t ex2_rate_probe(int iters, int nblocks, unsigned long long* out, cudaStream_t stream) {
+  constexpr int kPad = 120 * 1024;  // more than half an SM's shared memory: one CTA per SM
+  cudaError_t e = cudaFuncSetAttribute(ex2_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPad);
+  if (e != cudaSuccess) return e;
+  ex2_rate_kernel<<<nblocks, kEx2Threads, kPad, stream>>>(iters, out);
+  note_launches(1);
+  return cudaGetLastError();
+}
 
 cudaError_t wait_timeout_probe(uint64_t limit_ns, unsigned long long* elapsed, uint32_t* status, cudaStream_t stream) {
   wait_timeout_probe_kernel<<<1, 128, 0, stream>>>(limit_ns, elapsed, status);

@@ -26,7 +26,7 @@ EXPORTS = ("mcs_workspace_size", "mcs_group_pddp", "mcs_dense_attn", "mcs_anchor
            "mcs_selftest_tma_gather", "mcs_anchor_select_noalloc", "mcs_sparse_attn_gather_host",
            "mcs_sparse_attn_gather_host_workspace_size", "mcs_cache_entry_bytes", "mcs_cache_ring_create",
            "mcs_cache_ring_acquire", "mcs_cache_ring_release", "mcs_cache_ring_destroy",
-           "mcs_selftest_wait_timeout", "mcs_pddp_dirs_size", "mcs_group_pddp_warm")
+           "mcs_selftest_wait_timeout", "mcs_pddp_dirs_size", "mcs_group_pddp_warm", "mcs_selftest_ex2_rate")
 
 
 class McsError(RuntimeError):
@@ -77,6 +77,7 @@ def load(build_if_missing: bool = False):
         "mcs_selftest_tc_mma": (I, [P, P, P, I, ctypes.c_uint32, ctypes.c_uint32, S]),
         "mcs_selftest_tma_gather": (I, [P, I, P, P, S]),
         "mcs_selftest_wait_timeout": (I, [ctypes.c_uint64, P, S]),
+        "mcs_selftest_ex2_rate": (I, [I, I, P, S]),
         "mcs_anchor_select_noalloc": (I, [D, P, P, P, P, I, P, P, S]),
         "mcs_sparse_attn_gather_host": (I, [D, P, P, P, P, P, I, P, P, P, Z, I, S]),
         "mcs_sparse_attn_gather_host_workspace_size": (Z, [D, I]),
@@ -343,6 +344,24 @@ def mcs_selftest_wait_timeout(limit_ns, elapsed=None, stream=None):
     elapsed: optional int64 device tensor of one element receiving the wait in ns."""
     _check("mcs_selftest_wait_timeout", load().mcs_selftest_wait_timeout(int(limit_ns), _ptr(elapsed),
                                                                          _stream(stream)))
+
+
+def mcs_selftest_ex2_rate(iters, out, stream=None):
+    """Launch the exponential-rate diagnostic: out is an int64 device tensor [nblocks, 2]
+    receiving each CTA's duration in SM clock cycles and its exponential count."""
+    _check("mcs_selftest_ex2_rate", load().mcs_selftest_ex2_rate(int(iters), int(out.shape[0]), _ptr(out),
+                                                                 _stream(stream)))
+
+
+def ex2_per_clock_per_sm(iters=1 << 14):
+    """Exponentials (ex2.approx.ftz.f32) per SM clock cycle, median over one CTA per SM."""
+    import torch
+    n = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    out = torch.zeros((n, 2), dtype=torch.int64, device="cuda")
+    mcs_selftest_ex2_rate(iters, out)
+    mcs_check_status()
+    cyc, cnt = out[:, 0].double().cpu(), out[:, 1].double().cpu()
+    return float((cnt / cyc).median())
 
 
 def mcs_selftest_tma_gather(src, rows, out, stream=None):

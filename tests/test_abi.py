@@ -79,6 +79,10 @@ def test_bad_pointers_and_sizes_rejected(lib):
     assert lib.mcs_residual_apply(ctypes.byref(d), a, mis, a, None) == 1
     assert lib.mcs_anchor_residual(ctypes.byref(d), a, a, a, a, a, 10, None, a, None) == 1
     assert lib.mcs_selftest_tc_mma(a, a, a, 5, 0, 0, None) == 1
+    assert lib.mcs_selftest_ex2_rate(0, 1, a, None) == 1                # iters < 1
+    assert lib.mcs_selftest_ex2_rate(16, 0, a, None) == 1               # no CTA
+    assert lib.mcs_selftest_ex2_rate(16, 1, None, None) == 1            # no output
+    assert lib.mcs_selftest_ex2_rate(16, 1, ctypes.c_void_p(4096 + 4), None) == 1   # misaligned output
 
 
 def test_launch_counter_is_monotone(lib):

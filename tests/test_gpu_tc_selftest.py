@@ -63,3 +63,18 @@ def test_tma_gather4_rows(dev):
     ok = rows < 1000
     want[ok] = src[rows[ok].long()]
     assert torch.equal(out.cpu(), want)
+
+
+def test_ex2_rate(dev):
+    """The exponential-rate diagnostic: one CTA per SM, each reporting its SM
+    clock cycles and exponential count; the rate is positive, finite and of the
+    order an SM's special-function units allow (a few to a few tens per clock)."""
+    n = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = torch.zeros((n, 2), dtype=torch.int64, device=dev)
+    mcs.mcs_selftest_ex2_rate(1 << 12, out)
+    mcs.mcs_check_status()
+    cyc, cnt = out[:, 0].cpu(), out[:, 1].cpu()
+    assert bool((cyc > 0).all()) and bool((cnt == 1024 * 8 * (1 << 12)).all())
+    rate = mcs.ex2_per_clock_per_sm(1 << 12)
+    print(f"ex2.approx.ftz.f32 per SM clock: {rate:.2f}")
+    assert 2.0 < rate < 256.0

@@ -21,6 +21,9 @@ CASES = {
     "n600-d64-c128-k150": synth.Workload("t", 1, 1, (3, 10, 20), 64, "bf16", 128, "0.25", seed=7),
     "n1024-d128-c128-k205": synth.Workload("t", 2, 1, (2, 16, 32), 128, "bf16", 128, "0.2", seed=8),
     "n600-d128-c128-kN": synth.Workload("t", 1, 1, (3, 10, 20), 128, "bf16", 128, "1.0", seed=9),
+    # d = 64 with 16 key tiles per group: the deeper key/value rings wrap twice
+    "n4096-d64-c128-k2048": synth.Workload("t", 1, 1, (4, 32, 32), 64, "bf16", 128, "0.5", seed=11),
+    "n4000-d64-c64-k1500": synth.Workload("t", 1, 1, (4, 25, 40), 64, "bf16", 64, "0.375", seed=12),
     # one group per head (G = 1, 28 pad rows): no split at all, a key list shorter than one tile
     "n100-d128-c128-k30": synth.Workload("t", 1, 2, (1, 10, 10), 128, "bf16", 128, "0.3", seed=10),
 }
