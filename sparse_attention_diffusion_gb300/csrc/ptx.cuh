@@ -262,37 +262,6 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-// 2^x for a pair of fp32 values on the FMA pipe instead of the MUFU unit:
-// x = j + f with j = round(x) (adding 1.5 * 2^23 leaves j in the low mantissa
-// bits of t), 2^f from a degree-3 polynomial on [-1/2, 1/2] fitted here to
-// minimise the relative error (max 7.5e-5; coefficients from a Lawson-weighted
-// least-squares fit), and 2^j added into the exponent field as t_bits << 23.
-// Inputs below -126 are clamped to -126 (the result is then below 2^-125.5).
-__device__ __forceinline__ uint64_t f2_exp2_poly(uint64_t x2) {
-  constexpr float kShift = 12582912.f;  // 1.5 * 2^23
-  constexpr float c0 = 0.9999280571937561f, c1 = 0.6932609677314758f, c2 = 0.2426111251115799f,
-                  c3 = 0.0551716648042202f;
-  float a, b;
-  f2_unpack(x2, a, b);
-  const uint64_t x = f2_pack(fmaxf(a, -126.f), fmaxf(b, -126.f));
-  const uint64_t sh = f2_pack(kShift, kShift);
-  const uint64_t t = f2_add(x, sh);
-  const uint64_t f = f2_sub(x, f2_sub(t, sh));
-  uint64_t p = f2_fma(f, f2_pack(c3, c3), f2_pack(c2, c2));
-  p = f2_fma(p, f, f2_pack(c1, c1));
-  p = f2_fma(p, f, f2_pack(c0, c0));
-  uint32_t plo, phi, tlo, thi;
-  asm("mov.b64 {%0, %1}, %2;" : "=r"(plo), "=r"(phi) : "l"(p));
-  asm("mov.b64 {%0, %1}, %2;" : "=r"(tlo), "=r"(thi) : "l"(t));
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(plo + (tlo << 23)), "r"(phi + (thi << 23)));
-  return r;
-}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
