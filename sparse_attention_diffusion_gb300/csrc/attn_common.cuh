@@ -174,14 +174,16 @@ __device__ __forceinline__ bool softmax_rows_pp(int j0, int T, int nkv, uint32_t
   return ok;
 }
 
-// Epilogue of the split-KV form for one row, columns [C0, C1): O = fa O_a + fb O_b
+// Epilogue of the split-KV form for one row, columns [C0, C1) (rres: those columns
+// of the row's residual, or of O_dense for the residual store, loaded by the caller
+// ahead of time; unused by the plain epilogue): O = fa O_a + fb O_b
 // from TMEM (O_b skipped when use_b is false: its warpgroup saw no tile), then
 // as store_row. use_b must be uniform across the warp (the TMEM loads are
 // warp-collective); rows with tok < 0 load but store nothing.
 template <int kEpi, int C0, int C1>
 __device__ __forceinline__ void store_row_merged(uint32_t tOa, uint32_t tOb, bool use_b, uint32_t lane_off, int tok,
                                                  size_t rowoff, float fa, float fb, __nv_bfloat16* dst,
-                                                 const __nv_bfloat16* res_in) {
+                                                 const uint4 (&rres)[(C1 - C0) / 8]) {
 #pragma unroll
   for (int c = C0 / 32; c < C1 / 32; ++c) {
     uint32_t oa[32], ob[32];
@@ -198,7 +200,7 @@ __device__ __forceinline__ void store_row_merged(uint32_t tOa, uint32_t tOb, boo
         }
         const size_t off = rowoff + c * 32 + q4 * 8;
         if constexpr (kEpi != kEpiPlain) {
-          const uint4 rv = *reinterpret_cast<const uint4*>(res_in + off);
+          const uint4 rv = rres[(c * 32 + q4 * 8 - C0) / 8];
           const __nv_bfloat16* rb = reinterpret_cast<const __nv_bfloat16*>(&rv);
 #pragma unroll
           for (int i = 0; i < 8; ++i)

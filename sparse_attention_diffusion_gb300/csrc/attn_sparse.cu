@@ -156,6 +156,16 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
     }
     float m, l;
     bool ok = softmax_rows_pp<D>(w, T, nkv, tS, tO, lane_off, p.scale_log2, s_full + w, p_full + w, st, m, l);
+    // this warpgroup's half of the row's residual (or of O_dense), loaded while the
+    // last P V runs, so the epilogue does not wait on memory after o_done
+    uint4 rres[D / 16] = {};
+    if constexpr (kEpi != kEpiPlain) {
+      if (tok >= 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.res_in + (size_t(bh) * p.N + size_t(tok)) * D + w * (D / 2));
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) rres[i] = src[i];
+      }
+    }
     if (ok) ok = warp_all(mbar_wait(o_done, 0, st));
     // Both warpgroups must reach the exchange barrier, so a failed wait only
     // skips the stores. After o_done every MMA has completed and every copy has
@@ -176,9 +186,9 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
       const size_t rowoff = (size_t(bh) * p.N + size_t(tok < 0 ? 0 : tok)) * D;
       const uint32_t tO0 = tmem + L::kColO, tO1 = tmem + L::kColO + D;
       if (w == 0)
-        store_row_merged<kEpi, 0, D / 2>(tO0, tO1, T > 1, lane_off, tok, rowoff, f0 * inv, f1 * inv, dst, p.res_in);
+        store_row_merged<kEpi, 0, D / 2>(tO0, tO1, T > 1, lane_off, tok, rowoff, f0 * inv, f1 * inv, dst, rres);
       else
-        store_row_merged<kEpi, D / 2, D>(tO0, tO1, T > 1, lane_off, tok, rowoff, f0 * inv, f1 * inv, dst, p.res_in);
+        store_row_merged<kEpi, D / 2, D>(tO0, tO1, T > 1, lane_off, tok, rowoff, f0 * inv, f1 * inv, dst, rres);
     }
     if (!ok && row == 0) raise_status(st, kStatusTimeout);
   } else if (warp < 16) {
@@ -188,6 +198,18 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
     const int ch = t % kChunks, r0 = t / kChunks;
     const __nv_bfloat16* kb = p.k + size_t(bh) * p.N * D;
     const __nv_bfloat16* vb = p.v + size_t(bh) * p.N * D;
+    // This thread's key ids of tile i (its rows r0 + k * kRowsPerPass), -1 past
+    // the end of the list; read one tile ahead, so the loads complete while the
+    // leader waits for the stages.
+    auto load_ids = [&](int i, int (&ids)[kPasses]) {
+#pragma unroll
+      for (int it = 0; it < kPasses; ++it) {
+        const int slot = i * 128 + it * kRowsPerPass + r0;
+        ids[it] = slot < nkv ? __ldg(idxg + slot) : -1;
+      }
+    };
+    int ida[kPasses], idb[kPasses];  // ids of even / odd tiles (no copies between them)
+    load_ids(0, ida);  // tile 0's ids first: their loads overlap the query rows' copies
     {  // the group's query rows (through perm): operand A of S = Q K^T
       const __nv_bfloat16* qb = p.q + size_t(bh) * p.N * D;
       const int32_t* permg = p.perm + size_t(bh) * p.N_pad + size_t(g) * p.C;
@@ -207,16 +229,6 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
       }
       cp_async_arrive_noinc(q_full);
     }
-    // This thread's key ids of tile i (its rows r0 + k * kRowsPerPass), -1 past
-    // the end of the list; read one tile ahead, so the loads complete while the
-    // leader waits for the stages.
-    auto load_ids = [&](int i, int (&ids)[kPasses]) {
-#pragma unroll
-      for (int it = 0; it < kPasses; ++it) {
-        const int slot = i * 128 + it * kRowsPerPass + r0;
-        ids[it] = slot < nkv ? __ldg(idxg + slot) : -1;
-      }
-    };
     static_assert(kRowsPerPass % 8 == 0, "a thread's rows share one swizzle phase");
     const uint32_t doff = sw128_off(r0, ch);  // + it * kRowsPerPass * 128 for pass it
     const __nv_bfloat16* kbc = kb + ch * 8;
@@ -279,8 +291,6 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
       }
       return true;
     };
-    int ida[kPasses], idb[kPasses];  // ids of even / odd tiles (no copies between them)
-    load_ids(0, ida);
     bool ok = true;
     for (int i = 0; ok && i < T; i += 2) {
       ok = tile(i, ida, idb);
