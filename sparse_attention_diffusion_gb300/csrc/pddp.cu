@@ -7,7 +7,8 @@
 // n - floor(n/2) groups, so node k of level l is found by walking the bits of
 // k from the root. The current ordering `perm` keeps every node's members in a
 // contiguous, ascending run; a level
-//   1. sums the members of each chunk (<= 8 groups of one node) -> node mean,
+//   1. sums the members of each chunk (<= 8 groups of one node; one group on
+//      the fp64 path of a layer with few chunks) -> node mean,
 //   2. accumulates each chunk's centred covariance (d x d) -> node covariance,
 //   3. runs exactly `iters` power iterations w = Cov v, v = w/|w| from 1/sqrt(d),
 //   4. projects every member on v and turns the projection into an
@@ -31,7 +32,16 @@
 namespace mcs {
 namespace {
 
-constexpr int kChunkGroups = 8;  // groups per covariance chunk
+constexpr int kChunkGroups = 8;  // groups per moment chunk (the usual case)
+
+// Groups per moment chunk. A chunk is one CTA of the moment kernels; on the fp64
+// path (fp32 inputs) a layer with few chunks would leave most SMs idle on
+// fp64 arithmetic (the tiny 1,024-token head has 2 chunks of 8 groups per
+// level), so there every group is its own chunk while the chunks stay few
+// enough for the fp64 partial moments to stay small.
+inline int chunk_groups(int BH, int G, bool bf16) {
+  return (!bf16 && BH * ((G + kChunkGroups - 1) / kChunkGroups) < 256) ? 1 : kChunkGroups;
+}
 
 __host__ __device__ inline bool pddp_node(int G, int level, int k, int* start, int* n) {
   int s = 0, m = G;
@@ -56,11 +66,11 @@ int num_levels(int G) {
   return L;
 }
 
-int host_level_chunks(int G, int level) {
+int host_level_chunks(int G, int level, int cg) {
   int total = 0;
   for (int k = 0; k < (1 << level); ++k) {
     int s, n;
-    if (pddp_node(G, level, k, &s, &n) && n >= 2) total += (n + kChunkGroups - 1) / kChunkGroups;
+    if (pddp_node(G, level, k, &s, &n) && n >= 2) total += (n + cg - 1) / cg;
   }
   return total;
 }
@@ -73,6 +83,7 @@ struct Tables {
   int* chunk_node;   // [L][G]
   int* chunk_g0;     // [L][G]
   int* chunk_ng;     // [L][G]
+  int cg;            // groups per chunk
 };
 
 __global__ void __launch_bounds__(1024) tables_kernel(Tables t, int G) {
@@ -87,7 +98,7 @@ __global__ void __launch_bounds__(1024) tables_kernel(Tables t, int G) {
     int s = 0, n = 0;
     const bool exists = k < nodes && pddp_node(G, level, k, &s, &n);
     const bool active = exists && n >= 2;
-    const int nch = active ? (n + kChunkGroups - 1) / kChunkGroups : 0;
+    const int nch = active ? (n + t.cg - 1) / t.cg : 0;
     // exclusive prefix of nch over the block (nch <= G fits easily)
     int pre = 0, tot = 0;
     {
@@ -118,8 +129,8 @@ __global__ void __launch_bounds__(1024) tables_kernel(Tables t, int G) {
       for (int c = 0; c < nch; ++c) {
         const size_t co = size_t(level) * G + c0 + c;
         t.chunk_node[co] = k;
-        t.chunk_g0[co] = s + c * kChunkGroups;
-        t.chunk_ng[co] = min(kChunkGroups, n - c * kChunkGroups);
+        t.chunk_g0[co] = s + c * t.cg;
+        t.chunk_ng[co] = min(t.cg, n - c * t.cg);
       }
     }
     __syncthreads();
@@ -504,14 +515,16 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct WsLayout {
   size_t perm_tmp, keys, tables, psum, pcnt, node_mu, node_v, pcov, total;
   int L, max_chunks;
+  int cg;  // groups per moment chunk
 };
 
 WsLayout layout(int BH, int N_pad, int C, int G, int d, bool bf16) {
   WsLayout w{};
   const size_t asz = bf16 ? sizeof(float) : sizeof(double);
   w.L = num_levels(G);
+  w.cg = chunk_groups(BH, G, bf16);
   int mc = 1;
-  for (int l = 0; l < w.L; ++l) mc = std::max(mc, host_level_chunks(G, l));
+  for (int l = 0; l < w.L; ++l) mc = std::max(mc, host_level_chunks(G, l, w.cg));
   w.max_chunks = mc;
   size_t off = 0;
   w.perm_tmp = off; off = align256(off + size_t(BH) * N_pad * 4);
@@ -550,6 +563,7 @@ cudaError_t run_typed(const PddpProblem& p, uint8_t* ws, cudaStream_t s) {
   t.chunk_node = tb + 4 * TL;
   t.chunk_g0 = tb + 5 * TL;
   t.chunk_ng = tb + 6 * TL;
+  t.cg = w.cg;
   A* psum = reinterpret_cast<A*>(ws + w.psum);
   int* pcnt = reinterpret_cast<int*>(ws + w.pcnt);
   A* node_mu = reinterpret_cast<A*>(ws + w.node_mu);
@@ -568,7 +582,7 @@ cudaError_t run_typed(const PddpProblem& p, uint8_t* ws, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   for (int l = 0; l < w.L; ++l) {
     const int nodes = 1 << l;
-    const int nch = host_level_chunks(G, l);
+    const int nch = host_level_chunks(G, l, w.cg);
     const dim3 gc(nch, p.BH), gn(nodes, p.BH);
     int32_t* cur = bufs[l & 1];
     int32_t* nxt = bufs[(l + 1) & 1];
