@@ -357,11 +357,34 @@ __global__ void __launch_bounds__(256) power_kernel(Tables t, int level, int G, 
   __syncthreads();
   if (threadIdx.x < D) v[threadIdx.x] = node_v[(size_t(bh) * G + k) * D + threadIdx.x];
   __syncthreads();
+  // fp64 (fp32 inputs): a column's sum is split over the 256 / D threads that
+  // share it, each with four partial sums (fp64 FMAs are few per SM and a
+  // D-long dependent chain would be pure latency); the parts are added in a
+  // fixed order. fp32 accumulation keeps one in-order chain per column.
+  constexpr bool kSplit = std::is_same<A, double>::value;
+  constexpr int kH = kSplit ? 256 / D : 1, kJL = D / kH;
+  __shared__ A part[kH][D];
   for (int it = 0; it < iters; ++it) {
+    if constexpr (kSplit) {
+      const int col = threadIdx.x % D, hh = threadIdx.x / D;
+      A s4[4] = {A(0), A(0), A(0), A(0)};
+#pragma unroll
+      for (int jj = 0; jj < kJL; jj += 4) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) s4[q] += cov[(hh * kJL + jj + q) * D + col] * v[hh * kJL + jj + q];
+      }
+      part[hh][col] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+      __syncthreads();
+    }
     if (threadIdx.x < D) {
       // the covariance is exactly symmetric, so read column i (conflict-free)
       A s = 0;
-      for (int j = 0; j < D; ++j) s += cov[j * D + threadIdx.x] * v[j];
+      if constexpr (kSplit) {
+#pragma unroll
+        for (int i = 0; i < kH; ++i) s += part[i][threadIdx.x];
+      } else {
+        for (int j = 0; j < D; ++j) s += cov[j * D + threadIdx.x] * v[j];
+      }
       w[threadIdx.x] = s;
       A sq = s * s;
 #pragma unroll
