@@ -389,18 +389,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       }
       tc_fence_after();
       uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+      // this group's 128 columns, 32 at a time, the next chunk's load in flight
+      // while the current one is exponentiated
+      const uint32_t tcol = tmem + lane_off + b * 256 + gsel * 128;
+      auto chunk = [&](const uint32_t (&r)[32], int col) {
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {  // this group's 128 columns, 64 at a time
-        uint32_t r[64];
-        const int col = gsel * 128 + c * 64;
-        tmem_ld64(tmem + lane_off + b * 256 + col, r);
-        if (c == 1) {  // this warpgroup's part of the row is in registers
-          tc_fence_before();
-          mbar_arrive(s_free + b);
-        }
-#pragma unroll
-        for (int i = 0; i < 64; i += 4) {
-          const float4 nl = *reinterpret_cast<const float4*>(nlse + col + i);
+        for (int i = 0; i < 32; i += 4) {
+          const float4 nl = *reinterpret_cast<const float4*>(nlse + gsel * 128 + col + i);
           const uint64_t x01 = f2_fma(f2_pack(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), sl2x2, f2_pack(nl.x, nl.y));
           const uint64_t x23 =
               f2_fma(f2_pack(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])), sl2x2, f2_pack(nl.z, nl.w));
@@ -410,7 +405,22 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           acc[0] = f2_add(acc[0], f2_pack(ex2_approx(x0), ex2_approx(x1)));
           acc[1] = f2_add(acc[1], f2_pack(ex2_approx(x2), ex2_approx(x3)));
         }
-      }
+      };
+      uint32_t ra[32], rb[32];
+      tmem_ld32_nowait(tcol, ra);
+      tmem_wait_ld32(ra);
+      tmem_ld32_nowait(tcol + 32, rb);
+      chunk(ra, 0);
+      tmem_wait_ld32(rb);
+      tmem_ld32_nowait(tcol + 64, ra);
+      chunk(rb, 32);
+      tmem_wait_ld32(ra);
+      tmem_ld32_nowait(tcol + 96, rb);
+      chunk(ra, 64);
+      tmem_wait_ld32(rb);
+      tc_fence_before();  // this warpgroup's part of the row is in registers
+      mbar_arrive(s_free + b);
+      chunk(rb, 96);
       const int key = j * 128 + (tid & 127);
       if (mine && key < p.N) {
         float a0, a1;
