@@ -26,6 +26,8 @@ CASES = {
     "n4000-d64-c64-k1500": synth.Workload("t", 1, 1, (4, 25, 40), 64, "bf16", 64, "0.375", seed=12),
     # one group per head (G = 1, 28 pad rows): no split at all, a key list shorter than one tile
     "n100-d128-c128-k30": synth.Workload("t", 1, 2, (1, 10, 10), 128, "bf16", 128, "0.3", seed=10),
+    # d = 64, G = 2 (28 pad rows), one key tile per group: the odd-tile chain has nothing to issue
+    "n100-d64-c64-k30": synth.Workload("t", 1, 2, (1, 10, 10), 64, "bf16", 64, "0.3", seed=13),
 }
 
 
