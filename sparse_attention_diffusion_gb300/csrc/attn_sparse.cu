@@ -296,6 +296,31 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
       ok = tile(i, ida, idb);
       if (ok && i + 1 < T) ok = tile(i + 1, idb, ida);
     }
+    // Idle from here on: warm L2 with the first rows of the group whose CTA starts
+    // about one SM count later (its query rows through perm, the key and value
+    // rows of its first tile through its index list). Prefetches are hints: no
+    // data is read into the CTA and every address is checked first.
+    if (ok) {
+      uint32_t nsm;
+      asm("mov.u32 %0, %%nsmid;" : "=r"(nsm));
+      const long long nxt = (long long)bh * p.G + g + nsm;
+      if (nxt < (long long)p.BH * p.G) {
+        const int bh2 = int(nxt / p.G), g2 = int(nxt % p.G);
+        const int r = t >> 1, hh = t & 1;
+        if (hh < kHalves && r < 128) {
+          const int32_t* permg2 = p.perm + size_t(bh2) * p.N_pad + size_t(g2) * p.C;
+          const int32_t* idx2 = p.idx + (size_t(bh2) * p.G + g2) * size_t(p.K);
+          const int tq = r < p.C ? __ldg(permg2 + r) : -1;
+          const int tk = r < p.K ? __ldg(idx2 + r) : -1;
+          if (tq >= 0 && tq < p.N)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p.q + (size_t(bh2) * p.N + tq) * D + hh * 64));
+          if (tk >= 0 && tk < p.N) {
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p.k + (size_t(bh2) * p.N + tk) * D + hh * 64));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p.v + (size_t(bh2) * p.N + tk) * D + hh * 64));
+          }
+        }
+      }
+    }
     // let every copy land before the CTA can exit (normally long done)
     asm volatile("cp.async.wait_all;" ::: "memory");
     (void)ok;
