@@ -100,123 +100,6 @@ __device__ __forceinline__ bool softmax_rows(int T, int nkv, uint32_t tS, uint32
   return ok;
 }
 
-// Online base-2 softmax over every second tile, j = j0, j0 + 2, ... (the
-// split-KV form: two warpgroups take alternate key tiles of the same query rows,
-// each with its own S/P and O in tensor memory). The row of S_j is loaded into
-// registers, so the first 64 columns of the same buffer take P_j as bf16 pairs.
-// The MMA thread issues S_j into this buffer after P_{j-2} V_{j-2}, and the
-// completion of S_j covers that PV, so when S_j is seen O is stable and can be
-// rescaled at once. Same
-// lazy rescale (threshold 2^8) as softmax_rows. Returns false if a bounded wait
-// ran out; m, l describe the tiles this warpgroup saw (m = -inf, l = 0 if none).
-template <int D>
-__device__ __forceinline__ bool softmax_rows_pp(int j0, int T, int nkv, uint32_t tS, uint32_t tO, uint32_t lane_off,
-                                                float sl2, uint64_t* s_full, uint64_t* p_full, const uint32_t* st,
-                                                float& m_out, float& l_out) {
-  float m = -INFINITY, l = 0.f;
-  bool ok = true;
-  for (int j = j0, n = 0; j < T; j += 2, ++n) {
-    ok = warp_all(mbar_wait(s_full, uint32_t(n) & 1, st));
-    if (!ok) break;
-    tc_fence_after();
-    uint32_t r[128];
-    tmem_ld128(tS + lane_off, r);
-    const int nvalid = min(128, nkv - j * 128);
-    if (nvalid < 128) {  // last, partial tile: logits of missing keys become -inf (p = 0)
-#pragma unroll
-      for (int c = 0; c < 128; ++c)
-        if (c >= nvalid) r[c] = __float_as_uint(-INFINITY);
-    }
-    float mp[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) mp[i] = __uint_as_float(r[i]);
-#pragma unroll
-    for (int c = 8; c < 128; c += 2) mp[(c >> 1) & 7] = fmax3(mp[(c >> 1) & 7], __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
-    const float mx = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
-    const float m_new = fmaxf(m, mx * sl2);
-    const bool need = m_new > m + 8.f;
-    const float m_use = need ? m_new : m;
-    const float alpha = need ? ex2_approx(m - m_new) : 1.f;
-    const float neg_m = -m_use;
-    // two scores per packed FMA and two packed partial sums (four lanes)
-    const uint64_t sl2x2 = f2_pack(sl2, sl2), negmx2 = f2_pack(neg_m, neg_m);
-    uint64_t ls2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-    uint32_t pk[64];
-#pragma unroll
-    for (int c = 0; c < 64; ++c) {
-      float x0, x1;
-      f2_unpack(f2_fma(f2_pack(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])), sl2x2, negmx2), x0, x1);
-      const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-      ls2[c & 1] = f2_add(ls2[c & 1], f2_pack(p0, p1));
-      pk[c] = pack_bf16x2(p0, p1);
-    }
-    float la, lb;
-    f2_unpack(f2_add(ls2[0], ls2[1]), la, lb);
-    const float lsum = la + lb;
-    l = l * alpha + lsum;
-    m = m_use;
-    if (__any_sync(0xffffffffu, need && n > 0)) {
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tO + lane_off + c * 32, o);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        tmem_st32(tO + lane_off + c * 32, o);
-      }
-    }
-    tmem_st64(tS + lane_off, pk);
-    tc_fence_before();
-    mbar_arrive(p_full);
-  }
-  m_out = m;
-  l_out = l;
-  return ok;
-}
-
-// Epilogue of the split-KV form for one row, columns [C0, C1) (rres: those columns
-// of the row's residual, or of O_dense for the residual store, loaded by the caller
-// ahead of time; unused by the plain epilogue): O = fa O_a + fb O_b
-// from TMEM (O_b skipped when use_b is false: its warpgroup saw no tile), then
-// as store_row. use_b must be uniform across the warp (the TMEM loads are
-// warp-collective); rows with tok < 0 load but store nothing.
-template <int kEpi, int C0, int C1>
-__device__ __forceinline__ void store_row_merged(uint32_t tOa, uint32_t tOb, bool use_b, uint32_t lane_off, int tok,
-                                                 size_t rowoff, float fa, float fb, __nv_bfloat16* dst,
-                                                 const uint4 (&rres)[(C1 - C0) / 8]) {
-#pragma unroll
-  for (int c = C0 / 32; c < C1 / 32; ++c) {
-    uint32_t oa[32], ob[32];
-    tmem_ld32(tOa + lane_off + c * 32, oa);
-    if (use_b) tmem_ld32(tOb + lane_off + c * 32, ob);
-    if (tok >= 0 && dst != nullptr) {
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float o8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          o8[i] = __uint_as_float(oa[q4 * 8 + i]) * fa;
-          if (use_b) o8[i] = fmaf(__uint_as_float(ob[q4 * 8 + i]), fb, o8[i]);
-        }
-        const size_t off = rowoff + c * 32 + q4 * 8;
-        if constexpr (kEpi != kEpiPlain) {
-          const uint4 rv = rres[(c * 32 + q4 * 8 - C0) / 8];
-          const __nv_bfloat16* rb = reinterpret_cast<const __nv_bfloat16*>(&rv);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            o8[i] = (kEpi == kEpiAddResidual) ? o8[i] + __bfloat162float(rb[i]) : __bfloat162float(rb[i]) - o8[i];
-        }
-        uint4 wv;
-        wv.x = pack_bf16x2(o8[0], o8[1]);
-        wv.y = pack_bf16x2(o8[2], o8[3]);
-        wv.z = pack_bf16x2(o8[4], o8[5]);
-        wv.w = pack_bf16x2(o8[6], o8[7]);
-        *reinterpret_cast<uint4*>(dst + off) = wv;
-      }
-    }
-  }
-}
-
 // Epilogue for one row: O / l from TMEM, optionally plus (add-residual) or
 // subtracted from (store-residual) a bf16 row, rounded once to bf16 and stored.
 // Every thread of the warp must call it (the TMEM loads are warp-collective);
@@ -237,6 +120,39 @@ __device__ __forceinline__ void store_row(uint32_t tO, uint32_t lane_off, int to
         const size_t off = rowoff + c * 32 + q4 * 8;
         if constexpr (kEpi != kEpiPlain) {
           const uint4 rv = *reinterpret_cast<const uint4*>(res_in + off);
+          const __nv_bfloat16* rb = reinterpret_cast<const __nv_bfloat16*>(&rv);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            o8[i] = (kEpi == kEpiAddResidual) ? o8[i] + __bfloat162float(rb[i]) : __bfloat162float(rb[i]) - o8[i];
+        }
+        uint4 w;
+        w.x = pack_bf16x2(o8[0], o8[1]);
+        w.y = pack_bf16x2(o8[2], o8[3]);
+        w.z = pack_bf16x2(o8[4], o8[5]);
+        w.w = pack_bf16x2(o8[6], o8[7]);
+        *reinterpret_cast<uint4*>(dst + off) = w;
+      }
+    }
+  }
+}
+
+// store_row with the bf16 row to add (or subtract from) already in registers.
+template <int D, int kEpi>
+__device__ __forceinline__ void store_row_pre(uint32_t tO, uint32_t lane_off, int tok, size_t rowoff, float inv_l,
+                                              __nv_bfloat16* dst, const uint4 (&rres)[D / 8]) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32(tO + lane_off + c * 32, o);
+    if (tok >= 0 && dst != nullptr) {
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float o8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o8[i] = __uint_as_float(o[q4 * 8 + i]) * inv_l;
+        const size_t off = rowoff + c * 32 + q4 * 8;
+        if constexpr (kEpi != kEpiPlain) {
+          const uint4 rv = rres[c * 4 + q4];
           const __nv_bfloat16* rb = reinterpret_cast<const __nv_bfloat16*>(&rv);
 #pragma unroll
           for (int i = 0; i < 8; ++i)

@@ -6,42 +6,40 @@
 // residual (reuse step) or store R = O_dense - O_sparse (anchor step)
 // [MC-Sparse summary: residual paragraph].
 //
-// One CTA per group (kernels that hold tensor memory run one CTA per SM). The
-// key tiles of 128 keys are split between two softmax warpgroups (even tiles,
-// odd tiles), each with its own S/P and O accumulators in tensor memory, so the
-// tensor core works for one warpgroup while the other computes exponentials;
-// the two partial softmaxes are merged in the epilogue (max, rescale, sum).
-// 640 threads in five warpgroups:
-//   warpgroups 0-1 (warps 0-7)    softmax of even / odd tiles, one thread per
-//                                 query row; the merged epilogue (each
-//                                 warpgroup stores half of the columns);
-//   warpgroups 2-3 (warps 8-15)   eight gather warps: the group's query rows
+// One CTA per group (kernels that hold tensor memory run one CTA per SM), in the
+// structure of the dense kernel: one softmax warpgroup, S double-buffered in
+// tensor memory and P in its own columns, so S_{j+1} is computed while the
+// softmax of S_j runs and P_j V_j while the softmax of S_{j+1} runs; one thread
+// issues the S chain and another the P V chain. 512 threads in four warpgroups:
+//   warpgroup 0 (warps 0-3)       softmax, one thread per query row, and the
+//                                 epilogue (O / l plus or minus the row's
+//                                 residual, loaded while the last P V runs);
+//   warpgroups 1-2 (warps 4-11)   eight gather warps: the group's query rows
 //                                 (through perm) once, then per tile the key
 //                                 and value rows at the group's index list, as
 //                                 16-byte cp.async copies into 3-stage K and V
-//                                 rings (128-byte swizzled); eight threads per
-//                                 row, each copying one chunk of every 128-byte
-//                                 half, so a thread holds 4 row ids per tile;
-//   warpgroup 4 (warps 16-17)     tensor-memory allocation (warp 16) and the
-//                                 MMA schedules: lane 0 of warp 16 issues the
-//                                 even tiles' MMAs, lane 0 of warp 17 the odd
-//                                 tiles' (warps 18-19 idle).
+//                                 rings (6 stages at d = 64; 128-byte swizzled);
+//                                 eight threads per row, each copying one chunk
+//                                 of every 128-byte half, so a thread holds 4
+//                                 row ids per tile; once idle they prefetch into
+//                                 L2 the first rows of the group starting about
+//                                 one SM count later;
+//   warpgroup 3 (warps 12-13)     tensor-memory allocation and the S_j = Q K_j^T
+//                                 chain (lane 0 of warp 12), the O += P_j V_j
+//                                 chain (lane 0 of warp 13); warps 14-15 idle.
 // The gather warps never wait for their own copies: each thread ends a tile's
 // key (value) copies with an asynchronous arrive on the stage's full barrier,
-// which completes when every thread's rows have landed; the MMA thread then
-// fences the generic-to-async proxy before the tensor core reads them. The
+// which completes when every thread's rows have landed; the issuing threads
+// then fence the generic-to-async proxy before the tensor core reads them. The
 // gather warps only wait (through one leader and a named barrier) for the
 // stages to be released: a K stage when S of its tile is done, a V stage when
-// PV is done. Each gather thread reads its row indices for the next tile into
+// P V is done. Each gather thread reads its row indices for the next tile into
 // registers while the leader waits, and issues a tile's copies back to back.
-// Each of the two issuing threads serves one warpgroup's chain of tiles: S_c,
-// then P_j V_j followed by S_{j+2} (into that warpgroup's S buffer, whose first
-// columns held P_j), waiting on each operand's barrier in turn; a wait in one
-// chain never holds back the other's MMAs (one thread issuing both chains in a
-// fixed order measured 3.9 % slower at the 720p layer, 7.1 % at d = 64).
-// Tensor memory: S/P of warpgroup w at [128w, 128w+128) (P in the first 64
-// columns), O of warpgroup w at [256 + wD, 256 + wD + D).
-// Registers are rebalanced with setmaxnreg (softmax 176, gather 48, warpgroup 4
+// (A split-KV form, two softmax warpgroups taking alternate tiles with their
+// own S/P and O and a merged epilogue, measured 1.6 % slower at the 720p layer
+// and 1.3 % faster at d = 64.)
+// Tensor memory: S0 [0, 128), S1 [128, 256), O [256, 256 + D), P [384, 448).
+// Registers are rebalanced with setmaxnreg (softmax 200, gather 48, warpgroup 3
 // 32); the launcher checks that the split fits the registers the block is
 // launched with. All waits are bounded; on a timeout the CTA flags it, lets its
 // copies and MMAs land, frees tensor memory and returns.
@@ -54,25 +52,26 @@
 namespace mcs {
 namespace {
 
-constexpr int kSparseThreads = 640;
-constexpr int kGather = 256;   // gather threads (warpgroups 2-3)
-constexpr int kMmaWarp = 16;   // first warp of warpgroup 4
-constexpr int kRegSoftmax = 176, kRegGather = 48, kRegMma = 32;
-constexpr int kRegPool = 256 * kRegSoftmax + kGather * kRegGather + 128 * kRegMma;
+constexpr int kSparseThreads = 512;
+constexpr int kGather = 256;   // gather threads (warpgroups 1-2)
+constexpr int kMmaWarp = 12;   // first warp of warpgroup 3: TMEM allocation and the S chain
+constexpr int kPvWarp = 13;    // the P V chain
+constexpr int kRegSoftmax = 200, kRegGather = 48, kRegMma = 32;
+constexpr int kRegPool = 128 * kRegSoftmax + kGather * kRegGather + 128 * kRegMma;
 
 template <int D>
 struct SparseCfg {
-  static constexpr int kSK = 3, kSV = 3;      // K and V stages (equal: tile i's key and value rows go together)
+  static constexpr int kSK = D == 64 ? 6 : 3, kSV = kSK;  // K and V stages (equal: tile i's key and value rows go together)
   static constexpr int kTile = (D / 64) * kRegion;
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTile;
   static constexpr int kV = kK + kSK * kTile;
   static constexpr int kBar = kV + kSV * kTile;
-  static constexpr int kNumBars = 1 + 2 * kSK + 2 * kSV + 2 + 2 + 1 + 2;
+  static constexpr int kNumBars = 1 + 2 * kSK + 2 * kSV + 2 + 2 + 1 + 1 + 1 + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;  // tmem slot, stop flags [2]
   static constexpr int kBytes = kMisc + 32;
   static constexpr int kAlloc = kBytes + 1024;
-  static constexpr uint32_t kColO = 256;
+  static constexpr uint32_t kColO = 256, kColP = 384;  // S0, S1 at 0 and 128
   static_assert(kAlloc <= 227 * 1024, "shared memory");
 };
 
@@ -97,9 +96,11 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
   uint64_t* k_empty = k_full + SK;
   uint64_t* v_full = k_empty + SK;
   uint64_t* v_empty = v_full + SV;
-  uint64_t* s_full = v_empty + SV;  // [2] per warpgroup
-  uint64_t* p_full = s_full + 2;    // [2]
-  uint64_t* o_done = p_full + 2;
+  uint64_t* s_full = v_empty + SV;  // [2] S buffer b written
+  uint64_t* s_free = s_full + 2;    // [2] S buffer b read by the softmax
+  uint64_t* p_full = s_free + 2;    // P_j written
+  uint64_t* p_empty = p_full + 1;   // P_j V_j done (P free, O stable)
+  uint64_t* o_done = p_empty + 1;
   uint64_t* drain = o_done + 1;     // [2] one per issuing thread
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   // the gather leader's decision for iteration i lives in stop[i & 1]: a slow
@@ -123,10 +124,12 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
       mbar_init(v_full + s, kGather);
       mbar_init(v_empty + s, 1);
     }
-    for (int w = 0; w < 2; ++w) {
-      mbar_init(s_full + w, 1);
-      mbar_init(p_full + w, 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full + b, 1);
+      mbar_init(s_free + b, 128);
     }
+    mbar_init(p_full, 128);
+    mbar_init(p_empty, 1);
     mbar_init(o_done, 2);  // one commit from each issuing thread
     mbar_init(drain, 1);
     mbar_init(drain + 1, 1);
@@ -141,13 +144,11 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 8) {
+  if (warp < 4) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegSoftmax));
     // ------------------------------------------------------------ softmax, epilogue
-    const int w = warp >> 2;  // warpgroup: tiles w, w + 2, ...
-    const int row = tid & 127;
-    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + uint32_t(w * 128), tO = tmem + L::kColO + uint32_t(w * D);
+    const int row = tid;
+    const uint32_t lane_off = uint32_t(warp * 32) << 16;
     int tok = -1;
     if (row < p.C) {
       const int v = __ldg(p.perm + size_t(bh) * p.N_pad + size_t(g) * p.C + row);
@@ -155,46 +156,30 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
       else if (v < p.N) tok = v;
     }
     float m, l;
-    bool ok = softmax_rows_pp<D>(w, T, nkv, tS, tO, lane_off, p.scale_log2, s_full + w, p_full + w, st, m, l);
-    // this warpgroup's half of the row's residual (or of O_dense), loaded while the
-    // last P V runs, so the epilogue does not wait on memory after o_done
-    uint4 rres[D / 16] = {};
+    const SoftmaxSync sy{s_full, s_free, p_full, p_empty};
+    bool ok = softmax_rows<D, true>(T, nkv, tmem, tmem + L::kColO, tmem + L::kColP, lane_off, p.scale_log2, sy, st, m,
+                                    l);
+    // the row's residual (or O_dense), loaded while the last P V runs
+    uint4 rres[D / 8] = {};
     if constexpr (kEpi != kEpiPlain) {
       if (tok >= 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.res_in + (size_t(bh) * p.N + size_t(tok)) * D + w * (D / 2));
+        const uint4* src = reinterpret_cast<const uint4*>(p.res_in + (size_t(bh) * p.N + size_t(tok)) * D);
 #pragma unroll
-        for (int i = 0; i < D / 16; ++i) rres[i] = src[i];
+        for (int i = 0; i < D / 8; ++i) rres[i] = src[i];
       }
     }
     if (ok) ok = warp_all(mbar_wait(o_done, 0, st));
-    // Both warpgroups must reach the exchange barrier, so a failed wait only
-    // skips the stores. After o_done every MMA has completed and every copy has
-    // landed, so the first K stage holds the two warpgroups' (m, l) per row.
-    float2* ml = reinterpret_cast<float2*>(smem + L::kK);  // [2][128]
-    fence_proxy_async_smem();
-    ml[w * 128 + row] = make_float2(m, l);
-    named_bar_sync(2, 256);
-    const float2 other = ml[(w ^ 1) * 128 + row];
-    const float m0 = w == 0 ? m : other.x, l0 = w == 0 ? l : other.y;
-    const float m1 = w == 0 ? other.x : m, l1 = w == 0 ? other.y : l;
-    const float mm = fmaxf(m0, m1);
-    const float f0 = ex2_approx(m0 - mm), f1 = T > 1 ? ex2_approx(m1 - mm) : 0.f;
-    const float inv = 1.f / (l0 * f0 + l1 * f1);
     if (ok) {
       tc_fence_after();
       __nv_bfloat16* dst = (kEpi == kEpiStoreResidual) ? p.res_out : p.o;
       const size_t rowoff = (size_t(bh) * p.N + size_t(tok < 0 ? 0 : tok)) * D;
-      const uint32_t tO0 = tmem + L::kColO, tO1 = tmem + L::kColO + D;
-      if (w == 0)
-        store_row_merged<kEpi, 0, D / 2>(tO0, tO1, T > 1, lane_off, tok, rowoff, f0 * inv, f1 * inv, dst, rres);
-      else
-        store_row_merged<kEpi, D / 2, D>(tO0, tO1, T > 1, lane_off, tok, rowoff, f0 * inv, f1 * inv, dst, rres);
+      store_row_pre<D, kEpi>(tmem + L::kColO, lane_off, tok, rowoff, 1.f / l, dst, rres);
     }
     if (!ok && row == 0) raise_status(st, kStatusTimeout);
-  } else if (warp < 16) {
+  } else if (warp < 12) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegGather));
     // ------------------------------------------------------------ gather warps
-    const int t = tid - 256;  // 0..255
+    const int t = tid - 128;  // 0..255
     const int ch = t % kChunks, r0 = t / kChunks;
     const __nv_bfloat16* kb = p.k + size_t(bh) * p.N * D;
     const __nv_bfloat16* vb = p.v + size_t(bh) * p.N * D;
@@ -326,14 +311,13 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
     (void)ok;
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegMma));
-    // ------------------------------------------------------------ MMA issuers (warps 16, 17)
+    // ------------------------------------------------------------ MMA issuers (warps 12, 13)
     // Lane 0 of each runs its chain's schedule alone: its waits, MMAs and commits
-    // (the other lanes go straight to the final barrier; measured 2.4 % faster
-    // than the whole warp computing the operands with lane 0 issuing). Each
-    // thread's commits cover only its own MMAs, so o_done expects one commit
-    // from each, and each has its own drain barrier.
-    if ((warp == kMmaWarp || warp == kMmaWarp + 1) && lane == 0) {
-      const int chain = warp - kMmaWarp;  // this thread issues tiles chain, chain + 2, ...
+    // (the other lanes go straight to the final barrier). Each thread's commits
+    // cover only its own MMAs, so o_done expects one commit from each, and each
+    // has its own drain barrier.
+    if ((warp == kMmaWarp || warp == kPvWarp) && lane == 0) {
+      const bool pv_thread = warp == kPvWarp;
       constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
       bool ok = mbar_wait(q_full, 0, st);
@@ -343,51 +327,47 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
         tc_fence_after();
       }
       const uint32_t qlo = desc_lo_kmajor(sbase + L::kQ);
-      // Issue order of a chain: S_c, then P_j V_j followed by S_{j+2}: S_{j+2}
-      // writes the buffer that holds P_j, and the MMAs of this thread run in
-      // issue order, so the PV reads P before S_{j+2} overwrites it; the commit
-      // that tells the softmax S_{j+2} is done also covers that PV (O is stable
-      // when S_{j+2} is seen). The waits are blocking (bounded) waits.
-      auto issue_s = [&](int j) -> bool {
-        if (!mbar_wait(k_full + j % SK, uint32_t(j / SK) & 1, st)) return false;
-        fence_proxy_async_smem();  // key rows landed by cp.async, read by the tensor core
-        tc_fence_after();
-        const uint32_t klo = desc_lo_kmajor(sbase + L::kK + (j % SK) * L::kTile);
-        const uint32_t tS = tmem + uint32_t((j & 1) * 128);
+      if (!pv_thread) {
+        // S chain: S_j = Q K_j^T into S buffer j % 2 once the softmax has read S_{j-2}
+        for (int j = 0; ok && j < T; ++j) {
+          const int s = j % SK, b = j & 1;
+          ok = mbar_wait(k_full + s, uint32_t(j / SK) & 1, st) && mbar_wait(s_free + b, (uint32_t(j >> 1) & 1) ^ 1, st);
+          if (!ok) break;
+          fence_proxy_async_smem();  // key rows landed by cp.async, read by the tensor core
+          tc_fence_after();
+          const uint32_t klo = desc_lo_kmajor(sbase + L::kK + s * L::kTile);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          tc_mma_ss_lo(tS, qlo + kstep_kmajor(ks), klo + kstep_kmajor(ks), kIdescQK, ks > 0 ? 1u : 0u);
-        tc_commit(s_full + (j & 1));
-        tc_commit(k_empty + j % SK);
-        issued = true;
-        return true;
-      };
-      auto issue_pv = [&](int j) -> bool {
-        // P_j written by warpgroup j%2 and the value rows in
-        if (!(mbar_wait(p_full + (j & 1), uint32_t(j >> 1) & 1, st) &&
-              mbar_wait(v_full + j % SV, uint32_t(j / SV) & 1, st)))
-          return false;
-        fence_proxy_async_smem();  // value rows landed by cp.async
-        tc_fence_after();
-        const uint32_t vlo = desc_lo_mnmajor(sbase + L::kV + (j % SV) * L::kTile);
-        const uint32_t tP = tmem + uint32_t((j & 1) * 128), tO = tmem + L::kColO + uint32_t((j & 1) * D);
+          for (int ks = 0; ks < D / 16; ++ks)
+            tc_mma_ss_lo(tmem + uint32_t(b * 128), qlo + kstep_kmajor(ks), klo + kstep_kmajor(ks), kIdescQK,
+                         ks > 0 ? 1u : 0u);
+          tc_commit(s_full + b);
+          tc_commit(k_empty + s);
+          issued = true;
+        }
+      } else {
+        // P V chain: O += P_j V_j with P from its own tensor-memory columns
+        const uint32_t tO = tmem + L::kColO, tP = tmem + L::kColP;
+        for (int j = 0; ok && j < T; ++j) {
+          const int s = j % SV;
+          ok = mbar_wait(p_full, uint32_t(j) & 1, st) && mbar_wait(v_full + s, uint32_t(j / SV) & 1, st);
+          if (!ok) break;
+          fence_proxy_async_smem();  // value rows landed by cp.async
+          tc_fence_after();
+          const uint32_t vlo = desc_lo_mnmajor(sbase + L::kV + s * L::kTile);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          tc_mma_ts_lo(tO, tP + ks * 8, vlo + kstep_mnmajor(ks), kIdescPV, (j >= 2 || ks > 0) ? 1u : 0u);
-        tc_commit(v_empty + j % SV);
-        return true;
-      };
-      if (ok && chain < T) ok = issue_s(chain);
-      for (int j = chain; ok && j < T; j += 2) {
-        ok = issue_pv(j);
-        if (ok && j + 2 < T) ok = issue_s(j + 2);
+          for (int ks = 0; ks < 8; ++ks)
+            tc_mma_ts_lo(tO, tP + ks * 8, vlo + kstep_mnmajor(ks), kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
+          tc_commit(p_empty);
+          tc_commit(v_empty + s);
+          issued = true;
+        }
       }
       if (ok) tc_commit(o_done);
       if (!ok) {
         raise_status(st, kStatusTimeout);
         if (issued) {
-          tc_commit(drain + chain);
-          mbar_wait(drain + chain, 0, st);
+          tc_commit(drain + (pv_thread ? 1 : 0));
+          mbar_wait(drain + (pv_thread ? 1 : 0), 0, st);
         }
       }
     }
