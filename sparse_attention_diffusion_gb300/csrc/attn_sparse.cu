@@ -57,7 +57,8 @@ constexpr int kGather = 256;   // gather threads (warpgroups 1-2)
 constexpr int kMmaWarp = 12;   // first warp of warpgroup 3: TMEM allocation and the S chain
 constexpr int kPvWarp = 13;    // the P V chain
 constexpr int kRegSoftmax = 200, kRegGather = 48, kRegMma = 32;
-constexpr int kRegPool = 128 * kRegSoftmax + kGather * kRegGather + 128 * kRegMma;
+constexpr int kRegSoftmaxHalf = 240;  // the split-row epilogue needs more than 200 to stay out of local memory
+constexpr int reg_pool(bool half) { return 128 * (half ? kRegSoftmaxHalf : kRegSoftmax) + kGather * kRegGather + 128 * kRegMma; }
 
 template <int D>
 struct SparseCfg {
@@ -75,7 +76,7 @@ struct SparseCfg {
   static_assert(kAlloc <= 227 * 1024, "shared memory");
 };
 
-template <int D, int kEpi>
+template <int D, int kEpi, bool kHalf>
 __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const TcAttnParams p) {
   using L = SparseCfg<D>;
   constexpr int SK = L::kSK, SV = L::kSV;
@@ -145,20 +146,36 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegSoftmax));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kHalf ? kRegSoftmaxHalf : kRegSoftmax));
     // ------------------------------------------------------------ softmax, epilogue
+    // kHalf (C <= 64): query row r sits on lanes r and r + 64; lane r takes keys
+    // 0-63 of every tile and lane r + 64 keys 64-127, each with its own running
+    // max, sum and O row, merged in the epilogue. half is warp-uniform.
     const int row = tid;
+    const int half = kHalf ? row >> 6 : 0;
+    const int qrow = kHalf ? row & 63 : row;
     const uint32_t lane_off = uint32_t(warp * 32) << 16;
     int tok = -1;
-    if (row < p.C) {
-      const int v = __ldg(p.perm + size_t(bh) * p.N_pad + size_t(g) * p.C + row);
+    if (qrow < p.C) {
+      const int v = __ldg(p.perm + size_t(bh) * p.N_pad + size_t(g) * p.C + qrow);
       if (v < 0 || v >= p.N_pad) raise_status(st, kStatusBounds);
       else if (v < p.N) tok = v;
     }
+    if (half) tok = -1;  // lane r + 64 hands its partial row to lane r
     float m, l;
     const SoftmaxSync sy{s_full, s_free, p_full, p_empty};
-    bool ok = softmax_rows<D, true>(T, nkv, tmem, tmem + L::kColO, tmem + L::kColP, lane_off, p.scale_log2, sy, st, m,
-                                    l);
+    bool ok;
+    if constexpr (kHalf) {
+      // the other half's P columns stay zero for the whole group
+      uint32_t z[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = 0u;
+      tmem_st32(tmem + L::kColP + lane_off + uint32_t(32 - half * 32), z);
+      ok = softmax_rows<D, true, 64>(T, nkv, tmem, tmem + L::kColO, tmem + L::kColP, lane_off, p.scale_log2, sy, st, m,
+                                     l, half * 64);
+    } else {
+      ok = softmax_rows<D, true>(T, nkv, tmem, tmem + L::kColO, tmem + L::kColP, lane_off, p.scale_log2, sy, st, m, l);
+    }
     // the row's residual (or O_dense), loaded while the last P V runs
     uint4 rres[D / 8] = {};
     if constexpr (kEpi != kEpiPlain) {
@@ -169,10 +186,43 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
       }
     }
     if (ok) ok = warp_all(mbar_wait(o_done, 0, st));
-    if (ok) {
+    __nv_bfloat16* dst = (kEpi == kEpiStoreResidual) ? p.res_out : p.o;
+    const size_t rowoff = (size_t(bh) * p.N + size_t(tok < 0 ? 0 : tok)) * D;
+    if constexpr (kHalf) {
+      // Every tile has landed and every MMA is done (o_done), so the key ring's
+      // shared memory is free: lanes 64-127 leave their O rows there (float4 k of
+      // row r at k * 64 + r) with their max and sum; all 128 threads meet at the
+      // named barrier whatever their wait status.
+      float4* xo = reinterpret_cast<float4*>(smem + L::kK);
+      float* xm = reinterpret_cast<float*>(smem + L::kK + 64 * D * 4);
+      if (half) {
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tmem + L::kColO + lane_off + c * 32, o);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              xo[(c * 8 + k) * 64 + qrow] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                                        __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+          }
+        }
+        xm[qrow] = m;
+        xm[64 + qrow] = l;
+      }
+      named_bar_sync(2, 128);
+      if (!half && ok) {
+        tc_fence_after();
+        const float m1 = xm[qrow], l1 = xm[64 + qrow];
+        const float mm = fmaxf(m, m1);
+        const float a0 = m == -INFINITY ? 0.f : ex2_approx(m - mm);
+        const float a1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - mm);
+        const float inv = 1.f / (l * a0 + l1 * a1);
+        store_row_pair<D, kEpi>(tmem + L::kColO, lane_off, tok, rowoff, a0 * inv, a1 * inv, xo + qrow, dst, rres);
+      }
+    } else if (ok) {
       tc_fence_after();
-      __nv_bfloat16* dst = (kEpi == kEpiStoreResidual) ? p.res_out : p.o;
-      const size_t rowoff = (size_t(bh) * p.N + size_t(tok < 0 ? 0 : tok)) * D;
       store_row_pre<D, kEpi>(tmem + L::kColO, lane_off, tok, rowoff, 1.f / l, dst, rres);
     }
     if (!ok && row == 0) raise_status(st, kStatusTimeout);
@@ -201,9 +251,10 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
 #pragma unroll 4
       for (int it = 0; it < kPasses; ++it) {
         const int row = it * kRowsPerPass + r0;
+        const int qr = kHalf ? row & 63 : row;  // kHalf: rows r and r + 64 hold the same query
         int tq = -1;
-        if (row < p.C) {
-          const int v = __ldg(permg + row);
+        if (qr < p.C) {
+          const int v = __ldg(permg + qr);
           if (v < 0 || v >= p.N_pad) raise_status(st, kStatusBounds);
           else if (v < p.N) tq = v;
         }
@@ -380,17 +431,18 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
   }
 }
 
-template <int D, int kEpi>
+template <int D, int kEpi, bool kHalf>
 cudaError_t launch_sparse(const TcAttnParams& p, cudaStream_t stream) {
   using L = SparseCfg<D>;
-  auto kern = attn_sparse_kernel<D, kEpi>;
+  static_assert(64 * D * 4 + 2 * 64 * 4 <= L::kSK * L::kTile, "the merge buffer fits the key ring");
+  auto kern = attn_sparse_kernel<D, kEpi, kHalf>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   // setmaxnreg.inc waits for registers released by the other warpgroups: launch
   // only if the rebalanced split fits what the block is launched with
   cudaFuncAttributes fa;
   if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
-  if (fa.numRegs * kSparseThreads < kRegPool || fa.numRegs < kRegGather) return cudaErrorInvalidValue;
+  if (fa.numRegs * kSparseThreads < reg_pool(kHalf) || fa.numRegs < kRegGather) return cudaErrorInvalidValue;
   dim3 grid(p.tiles_per_head, p.BH);
   kern<<<grid, kSparseThreads, L::kAlloc, stream>>>(p);
   note_launches(1);
@@ -401,8 +453,10 @@ cudaError_t launch_sparse(const TcAttnParams& p, cudaStream_t stream) {
 
 cudaError_t tc_sparse_attn(int D, int epi, const TcAttnParams& p, int BH, cudaStream_t stream) {
   (void)BH;
-#define MCS_SPARSE_CASE(DD, EE) \
-  if (D == DD && epi == EE) return launch_sparse<DD, EE>(p, stream);
+  // a group of at most 64 queries splits every row's keys over two lanes
+#define MCS_SPARSE_CASE(DD, EE)                                          \
+  if (D == DD && epi == EE)                                              \
+    return p.C <= 64 ? launch_sparse<DD, EE, true>(p, stream) : launch_sparse<DD, EE, false>(p, stream);
   MCS_SPARSE_CASE(128, kEpiPlain)
   MCS_SPARSE_CASE(128, kEpiAddResidual)
   MCS_SPARSE_CASE(128, kEpiStoreResidual)

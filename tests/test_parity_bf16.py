@@ -28,6 +28,12 @@ CASES = {
     "n100-d128-c128-k30": synth.Workload("t", 1, 2, (1, 10, 10), 128, "bf16", 128, "0.3", seed=10),
     # d = 64, G = 2 (28 pad rows), one key tile per group: the odd-tile chain has nothing to issue
     "n100-d64-c64-k30": synth.Workload("t", 1, 2, (1, 10, 10), 64, "bf16", 64, "0.3", seed=13),
+    # C = 64 splits each row's keys over two lanes (keys 0-63 / 64-127 of every tile):
+    # exactly one half's worth of keys (the second lane sees none), one key past it,
+    # and a second tile holding a single key
+    "n600-d128-c64-k64": synth.Workload("t", 1, 1, (3, 10, 20), 128, "bf16", 64, "0.1066", seed=14),
+    "n600-d64-c64-k65": synth.Workload("t", 1, 2, (3, 10, 20), 64, "bf16", 64, "0.1075", seed=15),
+    "n600-d128-c64-k129": synth.Workload("t", 1, 1, (3, 10, 20), 128, "bf16", 64, "0.2149", seed=16),
 }
 
 

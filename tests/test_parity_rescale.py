@@ -23,6 +23,7 @@ CASES = {
     "d128-k0.5": synth.Workload("t", 1, 1, (2, 16, 32), 128, "bf16", 128, "0.5", seed=82),
     "d64-c64-k0.75": synth.Workload("t", 1, 1, (2, 16, 32), 64, "bf16", 64, "0.75", seed=83),
     "d64-c128-n4096": synth.Workload("t", 1, 1, (4, 32, 32), 64, "bf16", 128, "0.5", seed=84),
+    "d128-c64-k0.5": synth.Workload("t", 1, 1, (2, 16, 32), 128, "bf16", 64, "0.5", seed=85),
 }
 
 
