@@ -332,10 +332,21 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
       ok = tile(i, ida, idb);
       if (ok && i + 1 < T) ok = tile(i + 1, idb, ida);
     }
-    // Idle from here on: warm L2 with the first rows of the group whose CTA starts
-    // about one SM count later (its query rows through perm, the key and value
-    // rows of its first tile through its index list). Prefetches are hints: no
-    // data is read into the CTA and every address is checked first.
+    // Idle from here on, a few tiles before the epilogue: warm L2 with this
+    // group's residual (or O_dense) rows, which the epilogue reads, and with the
+    // first rows of the group whose CTA starts about one SM count later (its query
+    // rows through perm, the key and value rows of its first tile through its
+    // index list). Prefetches are hints: no data is read into the CTA and every
+    // address is checked first.
+    if (ok && kEpi != kEpiPlain) {
+      const int r = t >> 1, hh = t & 1;  // query row r of the group, 128-byte half hh
+      const int qr = kHalf ? r & 63 : r;
+      if (hh < kHalves && r < 128 && (!kHalf || r < 64) && qr < p.C) {
+        const int tq = __ldg(p.perm + size_t(bh) * p.N_pad + size_t(g) * p.C + qr);
+        if (tq >= 0 && tq < p.N)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(p.res_in + (size_t(bh) * p.N + tq) * D + hh * 64));
+      }
+    }
     if (ok) {
       uint32_t nsm;
       asm("mov.u32 %0, %%nsmid;" : "=r"(nsm));
