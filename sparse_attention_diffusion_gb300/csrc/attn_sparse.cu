@@ -14,6 +14,11 @@
 //   warpgroup 0 (warps 0-3)       softmax, one thread per query row, and the
 //                                 epilogue (O / l plus or minus the row's
 //                                 residual, loaded while the last P V runs);
+//                                 a group of at most 64 queries puts each query
+//                                 on two lanes (r and r + 64), which take keys
+//                                 0-63 and 64-127 of every tile with their own
+//                                 running max, sum and O row, merged through
+//                                 shared memory in the epilogue;
 //   warpgroups 1-2 (warps 4-11)   eight gather warps: the group's query rows
 //                                 (through perm) once, then per tile the key
 //                                 and value rows at the group's index list, as
@@ -22,8 +27,8 @@
 //                                 eight threads per row, each copying one chunk
 //                                 of every 128-byte half, so a thread holds 4
 //                                 row ids per tile; once idle they prefetch into
-//                                 L2 the first rows of the group starting about
-//                                 one SM count later;
+//                                 L2 the group's residual rows and the first rows
+//                                 of the group starting about one SM count later;
 //   warpgroup 3 (warps 12-13)     tensor-memory allocation and the S_j = Q K_j^T
 //                                 chain (lane 0 of warp 12), the O += P_j V_j
 //                                 chain (lane 0 of warp 13); warps 14-15 idle.
@@ -39,8 +44,8 @@
 // own S/P and O and a merged epilogue, measured 1.6 % slower at the 720p layer
 // and 1.3 % faster at d = 64.)
 // Tensor memory: S0 [0, 128), S1 [128, 256), O [256, 256 + D), P [384, 448).
-// Registers are rebalanced with setmaxnreg (softmax 200, gather 48, warpgroup 3
-// 32); the launcher checks that the split fits the registers the block is
+// Registers are rebalanced with setmaxnreg (softmax 200, 240 with two lanes per
+// query; gather 48, warpgroup 3 32); the launcher checks that the split fits the registers the block is
 // launched with. All waits are bounded; on a timeout the CTA flags it, lets its
 // copies and MMAs land, frees tensor memory and returns.
 #include "attn_common.cuh"
