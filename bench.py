@@ -47,10 +47,10 @@ METRIC = "sparse-attn ms/layer & TFLOP/s (frac of bf16 roofline) at density 0.15
 UNIT = "ms/layer"
 REUSE_PER_STEP = 9
 # DRAM bytes (read + write) of one reuse-kernel launch on the 40-head layer: an
-# 8-head ncu capture of the same kernel (dram__bytes_read.sum 1.0609 GB +
-# dram__bytes_write.sum 0.1488 GB per 8-head launch) scaled by heads (traffic
+# 8-head ncu capture of the same kernel (dram__bytes_read.sum 1.0875 GB +
+# dram__bytes_write.sum 0.1490 GB per 8-head launch) scaled by heads (traffic
 # grows in proportion). Set to None when the kernel changes.
-SPARSE_TRAFFIC_BYTES_H40 = (1.0609e9 + 0.1488e9) * 40 / 8
+SPARSE_TRAFFIC_BYTES_H40 = (1.0875e9 + 0.1490e9) * 40 / 8
 
 
 def parse():
@@ -73,6 +73,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer end-to-end leg (profiler launch lists of the timed steps only)")
     ap.add_argument("--heads", type=int, default=None, help="override H (smaller case for profiler captures)")
+    ap.add_argument("--group-size", type=int, choices=(64, 128), default=None,
+                    help="override C (the 64-query form of the sparse kernel, for profiler captures)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget (CPU seconds)")
     ap.add_argument("--ref-seconds", type=float, default=60.0,
                     help="--impl reference: total oracle budget over the warm-up and timed steps (CPU seconds)")
@@ -755,8 +757,9 @@ def run_mcs(args, wl, K):
                          "frac": achieved / pk["bf16_sus"],
                          "traffic": (SPARSE_TRAFFIC_BYTES_H40 * wl.H / 40
                                      if (SPARSE_TRAFFIC_BYTES_H40 is not None and wl.name == "kernel-bench-720p"
-                                         and wl.d == 128 and K == 15120) else None),
-                         "kernel": "attn_sparse_kernel<128, add-residual>",
+                                         and wl.d == 128 and wl.C == 128 and K == 15120) else None),
+                         "kernel": ("attn_sparse_cs_kernel" if wl.C > 64 else "attn_sparse_kernel")
+                                   + f"<{wl.d}, add-residual>",
                          "peak_kind": f"{pk['src']} sustained bf16",
                          "algorithmic": "4*B*H*N*K*d kept FLOPs per launch"},
             "stages_ms": {s: statistics.mean(v) for s, v in stage_ms.items()},
@@ -856,6 +859,8 @@ def main():
         wl = wl.with_(density=args.density)
     if args.heads:
         wl = wl.with_(H=args.heads)
+    if args.group_size:
+        wl = wl.with_(C=args.group_size)
     K = wl.K
     if args.impl == "reference":
         run_reference(args, wl, K)

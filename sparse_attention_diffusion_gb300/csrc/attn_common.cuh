@@ -143,43 +143,13 @@ __device__ __forceinline__ void store_row(uint32_t tO, uint32_t lane_off, int to
   }
 }
 
-// store_row with the bf16 row to add (or subtract from) already in registers.
-template <int D, int kEpi>
-__device__ __forceinline__ void store_row_pre(uint32_t tO, uint32_t lane_off, int tok, size_t rowoff, float inv_l,
-                                              __nv_bfloat16* dst, const uint4 (&rres)[D / 8]) {
-#pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
-    uint32_t o[32];
-    tmem_ld32(tO + lane_off + c * 32, o);
-    if (tok >= 0 && dst != nullptr) {
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float o8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o8[i] = __uint_as_float(o[q4 * 8 + i]) * inv_l;
-        const size_t off = rowoff + c * 32 + q4 * 8;
-        if constexpr (kEpi != kEpiPlain) {
-          const uint4 rv = rres[c * 4 + q4];
-          const __nv_bfloat16* rb = reinterpret_cast<const __nv_bfloat16*>(&rv);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            o8[i] = (kEpi == kEpiAddResidual) ? o8[i] + __bfloat162float(rb[i]) : __bfloat162float(rb[i]) - o8[i];
-        }
-        uint4 w;
-        w.x = pack_bf16x2(o8[0], o8[1]);
-        w.y = pack_bf16x2(o8[2], o8[3]);
-        w.z = pack_bf16x2(o8[4], o8[5]);
-        w.w = pack_bf16x2(o8[6], o8[7]);
-        *reinterpret_cast<uint4*>(dst + off) = w;
-      }
-    }
-  }
-}
-
 // Epilogue for a query row whose keys were split over two threads (lanes r and
 // r + 64, each with its own running max): o0 * f0 + o1 * f1, o0 from TMEM and o1
 // from shared memory (float4 k of the row at o1[k * 64]), where f0 and f1 hold
-// each half's weight 2^(m_half - m) and 1 / l; then as store_row_pre.
+// each half's weight 2^(m_half - m) and 1 / l; then plus (add-residual) or
+// subtracted from (store-residual) the bf16 row held in rres, rounded once to
+// bf16 and stored. Every thread of the warp must call it (the TMEM loads are
+// warp-collective); rows with tok < 0 load but store nothing.
 template <int D, int kEpi>
 __device__ __forceinline__ void store_row_pair(uint32_t tO, uint32_t lane_off, int tok, size_t rowoff, float f0, float f1,
                                                const float4* o1, __nv_bfloat16* dst, const uint4 (&rres)[D / 8]) {

@@ -7,47 +7,42 @@
 // [MC-Sparse summary: residual paragraph].
 //
 // One CTA per group (kernels that hold tensor memory run one CTA per SM), in the
-// structure of the dense kernel: one softmax warpgroup, S double-buffered in
-// tensor memory and P in its own columns, so S_{j+1} is computed while the
-// softmax of S_j runs and P_j V_j while the softmax of S_{j+1} runs; one thread
-// issues the S chain and another the P V chain. 512 threads in four warpgroups:
-//   warpgroup 0 (warps 0-3)       softmax, one thread per query row, and the
-//                                 epilogue (O / l plus or minus the row's
-//                                 residual, loaded while the last P V runs);
-//                                 a group of at most 64 queries puts each query
-//                                 on two lanes (r and r + 64), which take keys
-//                                 0-63 and 64-127 of every tile with their own
-//                                 running max, sum and O row, merged through
-//                                 shared memory in the epilogue;
-//   warpgroups 1-2 (warps 4-11)   eight gather warps: the group's query rows
-//                                 (through perm) once, then per tile the key
-//                                 and value rows at the group's index list, as
-//                                 16-byte cp.async copies into 3-stage K and V
-//                                 rings (6 stages at d = 64; 128-byte swizzled);
-//                                 eight threads per row, each copying one chunk
-//                                 of every 128-byte half, so a thread holds 4
-//                                 row ids per tile; once idle they prefetch into
-//                                 L2 the group's residual rows and the first rows
-//                                 of the group starting about one SM count later;
-//   warpgroup 3 (warps 12-13)     tensor-memory allocation and the S_j = Q K_j^T
-//                                 chain (lane 0 of warp 12), the O += P_j V_j
-//                                 chain (lane 0 of warp 13); warps 14-15 idle.
-// The gather warps never wait for their own copies: each thread ends a tile's
-// key (value) copies with an asynchronous arrive on the stage's full barrier,
-// which completes when every thread's rows have landed; the issuing threads
-// then fence the generic-to-async proxy before the tensor core reads them. The
-// gather warps only wait (through one leader and a named barrier) for the
-// stages to be released: a K stage when S of its tile is done, a V stage when
-// P V is done. Each gather thread reads its row indices for the next tile into
-// registers while the leader waits, and issues a tile's copies back to back.
-// (A split-KV form, two softmax warpgroups taking alternate tiles with their
-// own S/P and O and a merged epilogue, measured 1.6 % slower at the 720p layer
-// and 1.3 % faster at d = 64.)
-// Tensor memory: S0 [0, 128), S1 [128, 256), O [256, 256 + D), P [384, 448).
-// Registers are rebalanced with setmaxnreg (softmax 200, 240 with two lanes per
-// query; gather 48, warpgroup 3 32); the launcher checks that the split fits the registers the block is
-// launched with. All waits are bounded; on a timeout the CTA flags it, lets its
-// copies and MMAs land, frees tensor memory and returns.
+// structure of the dense kernel: S double-buffered in tensor memory, so S_{j+1}
+// is computed while the softmax of S_j runs and P_j V_j while the softmax of
+// S_{j+1} runs; one thread issues the S chain and another the P V chain; every
+// query row is shared by two softmax threads, each taking one half of every
+// tile's keys with its own running max, sum and O row, merged in the epilogue.
+// Two forms:
+//   attn_sparse_cs_kernel (C > 64, 640 threads): two softmax warpgroups on the
+//     same tensor-memory lanes, warpgroup h taking keys [64h, 64h + 64) into its
+//     own O accumulator and writing its P over the S columns it read; the P V
+//     of a tile is two four-MMA chains, and S buffer b is refilled once the P V
+//     of its tile is done. The two threads of a row each store half of the
+//     output columns;
+//   attn_sparse_kernel (C <= 64, 512 threads): one softmax warpgroup; query r
+//     sits on lanes r and r + 64 (the gather copies its row into both rows of
+//     the query tile), lane r taking keys 0-63 and lane r + 64 keys 64-127 of
+//     every tile, with P in its own columns (the other half's P columns stay
+//     zero); lanes 64-127 hand their O rows to lanes 0-63 through shared memory.
+// In both, eight gather warps copy the group's query rows (through perm) once,
+// then per tile the key and value rows at the group's index list, as 16-byte
+// cp.async copies into 3-stage K and V rings (6 stages at d = 64; 128-byte
+// swizzled); eight threads per row, each copying one chunk of every 128-byte
+// half, so a thread holds 4 row ids per tile; once idle they prefetch into L2
+// the group's residual rows and the first rows of the group starting about one
+// SM count later. The gather warps never wait for their own copies: each thread
+// ends a tile's key (value) copies with an asynchronous arrive on the stage's
+// full barrier, which completes when every thread's rows have landed; the
+// issuing threads then fence the generic-to-async proxy before the tensor core
+// reads them. The gather warps only wait (through one leader and a named
+// barrier) for the stages to be released: a K stage when S of its tile is done,
+// a V stage when P V is done. Each gather thread reads its row indices for the
+// next tile into registers while the leader waits, and issues a tile's copies
+// back to back. The epilogue's residual row is loaded while the last P V runs.
+// Registers are rebalanced with setmaxnreg; each launcher checks that the split
+// fits the registers the block is launched with. All waits are bounded; on a
+// timeout the CTA flags it, lets its copies and MMAs land, frees tensor memory
+// and returns.
 #include "attn_common.cuh"
 #include "attn_tc.h"
 #include "common.cuh"
@@ -57,13 +52,16 @@
 namespace mcs {
 namespace {
 
+// ---------------------------------------------------------------- two lanes per query (C <= 64)
+// warpgroup 0 softmax and epilogue, 1-2 gather, warp 12 tensor-memory
+// allocation and the S chain, warp 13 the P V chain. Tensor memory: S0 [0, 128),
+// S1 [128, 256), O [256, 256 + D), P [384, 448).
 constexpr int kSparseThreads = 512;
 constexpr int kGather = 256;   // gather threads (warpgroups 1-2)
 constexpr int kMmaWarp = 12;   // first warp of warpgroup 3: TMEM allocation and the S chain
 constexpr int kPvWarp = 13;    // the P V chain
-constexpr int kRegSoftmax = 200, kRegGather = 48, kRegMma = 32;
-constexpr int kRegSoftmaxHalf = 240;  // the split-row epilogue needs more than 200 to stay out of local memory
-constexpr int reg_pool(bool half) { return 128 * (half ? kRegSoftmaxHalf : kRegSoftmax) + kGather * kRegGather + 128 * kRegMma; }
+constexpr int kRegSoftmax = 240, kRegGather = 48, kRegMma = 32;  // the merge epilogue spills below 240
+constexpr int kRegPool = 128 * kRegSoftmax + kGather * kRegGather + 128 * kRegMma;
 
 template <int D>
 struct SparseCfg {
@@ -81,7 +79,7 @@ struct SparseCfg {
   static_assert(kAlloc <= 227 * 1024, "shared memory");
 };
 
-template <int D, int kEpi, bool kHalf>
+template <int D, int kEpi>
 __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const TcAttnParams p) {
   using L = SparseCfg<D>;
   constexpr int SK = L::kSK, SV = L::kSV;
@@ -151,14 +149,14 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kHalf ? kRegSoftmaxHalf : kRegSoftmax));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegSoftmax));
     // ------------------------------------------------------------ softmax, epilogue
-    // kHalf (C <= 64): query row r sits on lanes r and r + 64; lane r takes keys
-    // 0-63 of every tile and lane r + 64 keys 64-127, each with its own running
-    // max, sum and O row, merged in the epilogue. half is warp-uniform.
+    // Query row r sits on lanes r and r + 64; lane r takes keys 0-63 of every
+    // tile and lane r + 64 keys 64-127, each with its own running max, sum and O
+    // row, merged in the epilogue. half is warp-uniform.
     const int row = tid;
-    const int half = kHalf ? row >> 6 : 0;
-    const int qrow = kHalf ? row & 63 : row;
+    const int half = row >> 6;
+    const int qrow = row & 63;
     const uint32_t lane_off = uint32_t(warp * 32) << 16;
     int tok = -1;
     if (qrow < p.C) {
@@ -169,18 +167,14 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
     if (half) tok = -1;  // lane r + 64 hands its partial row to lane r
     float m, l;
     const SoftmaxSync sy{s_full, s_free, p_full, p_empty};
-    bool ok;
-    if constexpr (kHalf) {
-      // the other half's P columns stay zero for the whole group
+    {  // the other half's P columns stay zero for the whole group
       uint32_t z[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) z[i] = 0u;
       tmem_st32(tmem + L::kColP + lane_off + uint32_t(32 - half * 32), z);
-      ok = softmax_rows<D, true, 64>(T, nkv, tmem, tmem + L::kColO, tmem + L::kColP, lane_off, p.scale_log2, sy, st, m,
-                                     l, half * 64);
-    } else {
-      ok = softmax_rows<D, true>(T, nkv, tmem, tmem + L::kColO, tmem + L::kColP, lane_off, p.scale_log2, sy, st, m, l);
     }
+    bool ok = softmax_rows<D, true, 64>(T, nkv, tmem, tmem + L::kColO, tmem + L::kColP, lane_off, p.scale_log2, sy,
+                                        st, m, l, half * 64);
     // the row's residual (or O_dense), loaded while the last P V runs
     uint4 rres[D / 8] = {};
     if constexpr (kEpi != kEpiPlain) {
@@ -193,7 +187,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
     if (ok) ok = warp_all(mbar_wait(o_done, 0, st));
     __nv_bfloat16* dst = (kEpi == kEpiStoreResidual) ? p.res_out : p.o;
     const size_t rowoff = (size_t(bh) * p.N + size_t(tok < 0 ? 0 : tok)) * D;
-    if constexpr (kHalf) {
+    {
       // Every tile has landed and every MMA is done (o_done), so the key ring's
       // shared memory is free: lanes 64-127 leave their O rows there (float4 k of
       // row r at k * 64 + r) with their max and sum; all 128 threads meet at the
@@ -226,9 +220,6 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
         const float inv = 1.f / (l * a0 + l1 * a1);
         store_row_pair<D, kEpi>(tmem + L::kColO, lane_off, tok, rowoff, a0 * inv, a1 * inv, xo + qrow, dst, rres);
       }
-    } else if (ok) {
-      tc_fence_after();
-      store_row_pre<D, kEpi>(tmem + L::kColO, lane_off, tok, rowoff, 1.f / l, dst, rres);
     }
     if (!ok && row == 0) raise_status(st, kStatusTimeout);
   } else if (warp < 12) {
@@ -256,7 +247,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
 #pragma unroll 4
       for (int it = 0; it < kPasses; ++it) {
         const int row = it * kRowsPerPass + r0;
-        const int qr = kHalf ? row & 63 : row;  // kHalf: rows r and r + 64 hold the same query
+        const int qr = row & 63;  // rows r and r + 64 hold the same query
         int tq = -1;
         if (qr < p.C) {
           const int v = __ldg(permg + qr);
@@ -345,8 +336,8 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
     // address is checked first.
     if (ok && kEpi != kEpiPlain) {
       const int r = t >> 1, hh = t & 1;  // query row r of the group, 128-byte half hh
-      const int qr = kHalf ? r & 63 : r;
-      if (hh < kHalves && r < 128 && (!kHalf || r < 64) && qr < p.C) {
+      const int qr = r;
+      if (hh < kHalves && r < 64 && qr < p.C) {
         const int tq = __ldg(p.perm + size_t(bh) * p.N_pad + size_t(g) * p.C + qr);
         if (tq >= 0 && tq < p.N)
           asm volatile("prefetch.global.L2 [%0];" ::"l"(p.res_in + (size_t(bh) * p.N + tq) * D + hh * 64));
@@ -447,18 +438,18 @@ __global__ void __launch_bounds__(kSparseThreads, 1) attn_sparse_kernel(const Tc
   }
 }
 
-template <int D, int kEpi, bool kHalf>
+template <int D, int kEpi>
 cudaError_t launch_sparse(const TcAttnParams& p, cudaStream_t stream) {
   using L = SparseCfg<D>;
   static_assert(64 * D * 4 + 2 * 64 * 4 <= L::kSK * L::kTile, "the merge buffer fits the key ring");
-  auto kern = attn_sparse_kernel<D, kEpi, kHalf>;
+  auto kern = attn_sparse_kernel<D, kEpi>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   // setmaxnreg.inc waits for registers released by the other warpgroups: launch
   // only if the rebalanced split fits what the block is launched with
   cudaFuncAttributes fa;
   if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
-  if (fa.numRegs * kSparseThreads < reg_pool(kHalf) || fa.numRegs < kRegGather) return cudaErrorInvalidValue;
+  if (fa.numRegs * kSparseThreads < kRegPool || fa.numRegs < kRegGather) return cudaErrorInvalidValue;
   dim3 grid(p.tiles_per_head, p.BH);
   kern<<<grid, kSparseThreads, L::kAlloc, stream>>>(p);
   note_launches(1);
@@ -822,10 +813,11 @@ cudaError_t launch_sparse_cs(const TcAttnParams& p, cudaStream_t stream) {
 
 cudaError_t tc_sparse_attn(int D, int epi, const TcAttnParams& p, int BH, cudaStream_t stream) {
   (void)BH;
-  // a group of at most 64 queries splits every row's keys over two lanes
+  // groups of more than 64 queries: two softmax warpgroups per row; of at most
+  // 64: two lanes per query
 #define MCS_SPARSE_CASE(DD, EE)                                          \
   if (D == DD && epi == EE)                                              \
-    return p.C <= 64 ? launch_sparse<DD, EE, true>(p, stream) : launch_sparse_cs<DD, EE>(p, stream);
+    return p.C <= 64 ? launch_sparse<DD, EE>(p, stream) : launch_sparse_cs<DD, EE>(p, stream);
   MCS_SPARSE_CASE(128, kEpiPlain)
   MCS_SPARSE_CASE(128, kEpiAddResidual)
   MCS_SPARSE_CASE(128, kEpiStoreResidual)

@@ -25,8 +25,9 @@ MASS_TOL = 1e-5
 # fraction of identical groups must reach these floors, and a split may only
 # differ where the oracle's own key gap at the rank boundary is at most
 # PDDP_GAP_MAX standard deviations of the node's keys. Measured on a GB300: every
-# bf16 parity layer and the nine sampled full-size heads (720p, 480p and
-# 118,800-token layers) agree with the oracle on every group, so the floors are 1.
+# bf16 parity layer and the fifteen sampled full-size heads (720p, 480p and
+# 118,800-token layers, and the 65,536-token sweep layer with 64-query groups at
+# both head dims) agree with the oracle on every group, so the floors are 1.
 PDDP_AGREE_FLOOR_SMALL = 1.0
 PDDP_AGREE_FLOOR_FULLSIZE = 1.0
 PDDP_GAP_MAX = 1e-2

@@ -1,8 +1,9 @@
 """Full-size layers in the launch configuration the benchmark uses: the 720p
 kernel-benchmark layer (B=1, H=40, N=75,600 on a 21x45x80 grid, d=128, bf16,
-C=128, K=15,120), the Wan2.1-1.3B-shaped 480p layer (H=12, N=32,768, K=6,554)
-and the 118,800-token schedule layer (H=24, 929 groups with 112 pad rows,
-K=17,820). The whole path runs on the GPU (grouping, dense attention + LSE,
+C=128, K=15,120), the Wan2.1-1.3B-shaped 480p layer (H=12, N=32,768, K=6,554),
+the 118,800-token schedule layer (H=24, 929 groups with 112 pad rows,
+K=17,820) and the density sweep's layer (H=16, N=65,536, K=13,108) with
+64-query groups at d = 128 and d = 64. The whole path runs on the GPU (grouping, dense attention + LSE,
 pass-2 selection, anchor residual, one drifted reuse step), and sampled heads,
 groups and rows are checked one by one against the float64 oracle fed the very
 tensors the GPU received (the oracle cannot run a whole layer in a test)."""
@@ -22,6 +23,10 @@ LAYERS = {
     "kernel-bench-720p": synth.KBENCH_720P,
     "wan2.1-1.3b-480p": synth.WAN13_480P,
     "schedule-118800": synth.SCHEDULE_HY,
+    # the density sweep's 65,536-token layer with 64-query groups (each query on two
+    # lanes of the sparse kernel), at both head dims, density 0.2
+    "sweep-65536-d128-c64": synth.SWEEP.with_(C=64),
+    "sweep-65536-d64-c64": synth.SWEEP.with_(d=64, C=64),
 }
 
 
