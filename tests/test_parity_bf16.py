@@ -34,6 +34,12 @@ CASES = {
     "n600-d128-c64-k64": synth.Workload("t", 1, 1, (3, 10, 20), 128, "bf16", 64, "0.1066", seed=14),
     "n600-d64-c64-k65": synth.Workload("t", 1, 2, (3, 10, 20), 64, "bf16", 64, "0.1075", seed=15),
     "n600-d128-c64-k129": synth.Workload("t", 1, 1, (3, 10, 20), 128, "bf16", 64, "0.2149", seed=16),
+    # C = 128 splits every tile's keys over two softmax warpgroups (keys 0-63 / 64-127):
+    # exactly the first half (the second warpgroup never sees a key), one key past it,
+    # and a last tile whose second half is empty
+    "n600-d128-c128-k64": synth.Workload("t", 1, 1, (3, 10, 20), 128, "bf16", 128, "0.1066", seed=17),
+    "n600-d128-c128-k65": synth.Workload("t", 1, 2, (3, 10, 20), 128, "bf16", 128, "0.1075", seed=18),
+    "n600-d64-c128-k129": synth.Workload("t", 1, 1, (3, 10, 20), 64, "bf16", 128, "0.2149", seed=19),
 }
 
 
