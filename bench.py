@@ -47,10 +47,10 @@ METRIC = "sparse-attn ms/layer & TFLOP/s (frac of bf16 roofline) at density 0.15
 UNIT = "ms/layer"
 REUSE_PER_STEP = 9
 # DRAM bytes (read + write) of one reuse-kernel launch on the 40-head layer: an
-# 8-head ncu capture of the same kernel (dram__bytes_read.sum 1.0875 GB +
-# dram__bytes_write.sum 0.1490 GB per 8-head launch) scaled by heads (traffic
+# 8-head ncu capture of the same kernel (dram__bytes_read.sum 1.0906 GB +
+# dram__bytes_write.sum 0.1489 GB per 8-head launch) scaled by heads (traffic
 # grows in proportion). Set to None when the kernel changes.
-SPARSE_TRAFFIC_BYTES_H40 = (1.0875e9 + 0.1490e9) * 40 / 8
+SPARSE_TRAFFIC_BYTES_H40 = (1.0906e9 + 0.1489e9) * 40 / 8
 
 
 def parse():
