@@ -758,8 +758,8 @@ def run_mcs(args, wl, K):
                          "traffic": (SPARSE_TRAFFIC_BYTES_H40 * wl.H / 40
                                      if (SPARSE_TRAFFIC_BYTES_H40 is not None and wl.name == "kernel-bench-720p"
                                          and wl.d == 128 and wl.C == 128 and K == 15120) else None),
-                         "kernel": ("attn_sparse_cs_kernel" if wl.C > 64 else "attn_sparse_kernel")
-                                   + f"<{wl.d}, add-residual>",
+                         "kernel": f"attn_sparse_cs_kernel<{wl.d}, add-residual, "
+                                   + ("64-query groups>" if wl.C <= 64 else "128-query groups>"),
                          "peak_kind": f"{pk['src']} sustained bf16",
                          "algorithmic": "4*B*H*N*K*d kept FLOPs per launch"},
             "stages_ms": {s: statistics.mean(v) for s, v in stage_ms.items()},
