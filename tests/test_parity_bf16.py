@@ -40,6 +40,10 @@ CASES = {
     "n600-d128-c128-k64": synth.Workload("t", 1, 1, (3, 10, 20), 128, "bf16", 128, "0.1066", seed=17),
     "n600-d128-c128-k65": synth.Workload("t", 1, 2, (3, 10, 20), 128, "bf16", 128, "0.1075", seed=18),
     "n600-d64-c128-k129": synth.Workload("t", 1, 1, (3, 10, 20), 64, "bf16", 128, "0.2149", seed=19),
+    # one selected key per group: the sparse output is that key's value row, and all
+    # but one softmax thread of a row see no key
+    "n600-d128-c128-k1": synth.Workload("t", 1, 1, (3, 10, 20), 128, "bf16", 128, "0.001", seed=20),
+    "n600-d64-c64-k1": synth.Workload("t", 1, 1, (3, 10, 20), 64, "bf16", 64, "0.001", seed=21),
 }
 
 
